@@ -1,0 +1,170 @@
+/*
+ * gdn.h -- C ABI of the KDA / Gated DeltaNet step on NVIDIA GB300 (sm_103a).
+ *
+ * The step (per sequence b, per token t, per value head h), as stated in
+ * "Thirty tiny kernels per layer" (the decode-step list and the pure step
+ * function) and in the delta-rule definition of Kimi Delta Attention /
+ * Gated DeltaNet:
+ *   1. X = [conv_state[b] (K-1 rows, oldest first); qkv[b,t]];
+ *      xhat[c] = silu(sum_j conv_w[c][j] * X[j][c]); conv_state[b] = X[1..K-1]
+ *   2. q, k, v = split(xhat) (channel order: q of every qk head, k of every qk
+ *      head, v of every value head); q <- q * q_scale / sqrt(|q|^2 + eps_l2),
+ *      k <- k / sqrt(|k|^2 + eps_l2).  Value head h reads qk head h / (H_v/H_qk).
+ *   3. g = -exp(A_log[h]) * softplus(f + dt_bias)  (per key channel for
+ *      GDN_GATE_PER_CHANNEL, one per head for GDN_GATE_PER_HEAD); alpha = exp(g)
+ *   4. beta = sigmoid(beta_logit)
+ *   5. S <- (I - beta k k^T) Diag(alpha) S + beta k v^T     (S is [d_k, d_v], fp32)
+ *   6. o = S^T q
+ *   7. y = o / sqrt(mean(o^2) + eps_norm) * norm_w * silu(z)
+ *
+ * Ownership: the caller owns every buffer.  The library allocates nothing,
+ * keeps no state between calls, makes no host<->device copy and never
+ * synchronises: work is queued on `stream` in stream order.  Every pointer is
+ * a device pointer.  state, state_hist, conv_w and out must be 16-byte
+ * aligned; every other pointer must be aligned to its element size.
+ *
+ * Errors: argument and shape errors return a negative status before anything
+ * is launched.  A failed launch returns GDN_ERR_CUDA (the CUDA error is left
+ * for cudaGetLastError).  Faults inside a kernel surface at the caller's next
+ * synchronisation.  There is no CPU fallback: a shape without a GPU kernel
+ * returns GDN_ERR_UNSUPPORTED.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = -1,        /* a required pointer is NULL                       */
+    GDN_ERR_ALIGN = -2,       /* a pointer is misaligned (see Ownership)         */
+    GDN_ERR_SHAPE = -3,       /* sizes are negative, inconsistent or out of range */
+    GDN_ERR_UNSUPPORTED = -4, /* valid, but no kernel instance for these sizes    */
+    GDN_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required       */
+    GDN_ERR_CUDA = -6,        /* the CUDA runtime refused a launch                */
+    GDN_ERR_TIMEOUT = -7      /* reserved: a bounded device wait gave up          */
+} gdn_status_t;
+
+typedef enum {
+    GDN_GATE_PER_HEAD = 0,    /* Gated DeltaNet: f [B,T,H_v],     dt_bias [H_v]     */
+    GDN_GATE_PER_CHANNEL = 1  /* KDA:            f [B,T,H_v,d_k], dt_bias [H_v,d_k] */
+} gdn_gate_mode_t;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
+
+/* Launch flags (gdn_shape_t.flags). */
+enum {
+    /*
+     * Launch with programmatic dependent launch: the kernel reads `state`,
+     * `conv_state` and the parameters before it waits for the previous kernel
+     * on the stream, and lets the next kernel start early.  The caller
+     * asserts that the kernel queued just before this call on the stream does
+     * not write `state`, `conv_state` or the parameters (for example, the
+     * previous layer of a model).  Inputs q/k/v/f/beta/z are read after the
+     * wait.  Without this flag launches are plain stream-ordered.
+     */
+    GDN_FLAG_PDL = 1
+};
+
+typedef struct {
+    int32_t B;          /* sequences                                              */
+    int32_t T;          /* tokens per sequence in this call                       */
+    int32_t H_qk;       /* query/key heads                                        */
+    int32_t H_v;        /* value heads, a multiple of H_qk                        */
+    int32_t d_k;        /* key width (state rows)                                 */
+    int32_t d_v;        /* value width (state columns)                            */
+    int32_t conv_K;     /* conv taps; conv_state keeps conv_K - 1 rows            */
+    int32_t chunk;      /* chunk length of gdn_prefill_chunked (64)               */
+    int32_t gate_mode;  /* gdn_gate_mode_t                                        */
+    int32_t in_dtype;   /* gdn_dtype_t of qkv, f, beta, z                         */
+    int32_t out_dtype;  /* gdn_dtype_t of out                                     */
+    int32_t flags;      /* GDN_FLAG_*                                             */
+    float q_scale;      /* d_k^-1/2 rounded to fp32 by the caller                 */
+    float eps_l2;       /* epsilon of the q/k L2 norm                             */
+    float eps_norm;     /* epsilon of the gated RMSNorm                           */
+} gdn_shape_t;
+
+/*
+ * Tensors, all row-major and contiguous.  C = 2*H_qk*d_k + H_v*d_v.
+ */
+typedef struct {
+    const void *qkv;       /* [B,T,C] in_dtype: pre-conv q|k|v rows               */
+    const void *f;         /* [B,T,H_v,d_k] or [B,T,H_v] in_dtype: gate logits    */
+    const void *beta;      /* [B,T,H_v] in_dtype: beta logits                     */
+    const void *z;         /* [B,T,H_v,d_v] in_dtype: output-gate rows            */
+    const float *conv_w;   /* [C,conv_K]                                          */
+    const float *A_log;    /* [H_v]                                               */
+    const float *dt_bias;  /* [H_v,d_k] or [H_v]                                  */
+    const float *norm_w;   /* [d_v]                                               */
+    float *conv_state;     /* [B,conv_K-1,C], oldest row first                    */
+    float *state;          /* [B,H_v,d_k,d_v]; row = key channel                  */
+    void *out;             /* [B,T,H_v*d_v] out_dtype                             */
+    float *state_hist;     /* verify: [T,B,H_v,d_k,d_v]; otherwise unused         */
+    float *conv_hist;      /* verify: [T,B,conv_K-1,C] or NULL; otherwise unused  */
+} gdn_tensors_t;
+
+/*
+ * One decode step (T must be 1): steps 1-7 for every sequence and value head.
+ * conv_state and state are advanced in place; out receives y.
+ * Kernel instances: d_k == d_v in {16, 32, 64, 128}, conv_K == 4.
+ */
+GDN_API gdn_status_t gdn_decode_step(const gdn_shape_t *shape, const gdn_tensors_t *t,
+                             gdn_stream_t stream);
+
+/*
+ * Multi-token verify (1 <= T <= 4): steps 1-7 for tokens 0..T-1 in order, as T
+ * decode steps would (the arithmetic per token is the decode step's, so the
+ * outputs and per-token states equal T gdn_decode_step calls bit for bit).
+ * state and conv_state are only read.  state_hist[t] receives the state after
+ * token t; conv_hist[t], when not NULL, the conv window after token t.  To
+ * commit k accepted tokens the caller adopts state_hist[k-1] and conv_hist[k-1]
+ * ("opus_gdn_qsa" audit, the gdn_step commit / verify modes and history output).
+ */
+GDN_API gdn_status_t gdn_verify_T(const gdn_shape_t *shape, const gdn_tensors_t *t,
+                          gdn_stream_t stream);
+
+/*
+ * Chunked prefill of T >= 1 tokens per sequence: the same result as T decode
+ * steps, computed in the chunked WY/UT form ("llama.cpp PR #84", chunked
+ * KDA prefill) with chunk length shape->chunk.  conv_state and state are
+ * advanced in place; out receives y for every token.  workspace must hold
+ * gdn_prefill_workspace_bytes(shape) bytes (may be 0 bytes; then NULL is
+ * accepted).
+ */
+GDN_API gdn_status_t gdn_prefill_chunked(const gdn_shape_t *shape, const gdn_tensors_t *t,
+                                 void *workspace, size_t workspace_bytes,
+                                 gdn_stream_t stream);
+
+/* Bytes of device workspace gdn_prefill_chunked needs for this shape (0 on a bad shape). */
+GDN_API size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
+
+/* Static, NUL-terminated name of a status code. */
+GDN_API const char *gdn_status_string(gdn_status_t status);
+
+/*
+ * Name of the kernel variant a call with this shape would launch for `op`
+ * (0 decode, 1 verify, 2 prefill), e.g. "step<128,16>" (d = 128, 16-column slabs).  Lets tests check that
+ * the intended fast path runs.  Returns NULL for an unsupported shape.
+ */
+GDN_API const char *gdn_kernel_variant(const gdn_shape_t *shape, int op);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,206 @@
+// C ABI of the KDA / Gated DeltaNet step: argument validation and dispatch.
+// Every check runs on the host before anything is queued; nothing here
+// allocates, copies or synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+#include "gdn_prefill.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_num_sms[kMaxDevices];  // 0 = not queried yet; benign race: every writer stores the same value
+
+int num_sms_current()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_num_sms[dev] = n;
+    }
+    return g_num_sms[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point (T is checked by the caller).
+gdn_status_t check_shape(const gdn_shape_t *s)
+{
+    if (!s) return GDN_ERR_NULL;
+    if (s->B < 0 || s->T < 0 || s->H_qk <= 0 || s->H_v <= 0 || s->d_k <= 0 || s->d_v <= 0)
+        return GDN_ERR_SHAPE;
+    if (s->H_v % s->H_qk != 0) return GDN_ERR_SHAPE;
+    if (s->B > 65535 || s->H_v > 65535) return GDN_ERR_SHAPE;
+    if (s->gate_mode != GDN_GATE_PER_HEAD && s->gate_mode != GDN_GATE_PER_CHANNEL)
+        return GDN_ERR_SHAPE;
+    if ((s->in_dtype != GDN_F32 && s->in_dtype != GDN_BF16) ||
+        (s->out_dtype != GDN_F32 && s->out_dtype != GDN_BF16))
+        return GDN_ERR_SHAPE;
+    if (s->flags & ~GDN_FLAG_PDL) return GDN_ERR_SHAPE;
+    if (!(s->q_scale > 0.0f) || !(s->eps_l2 >= 0.0f) || !(s->eps_norm >= 0.0f))
+        return GDN_ERR_SHAPE;
+    if (s->conv_K != 4) return GDN_ERR_UNSUPPORTED;
+    if (s->d_k != s->d_v) return GDN_ERR_UNSUPPORTED;
+    const long C = 2L * s->H_qk * s->d_k + static_cast<long>(s->H_v) * s->d_v;
+    if (C > (1L << 30)) return GDN_ERR_SHAPE;
+    return GDN_OK;
+}
+
+bool aligned(const void *p, unsigned bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
+
+// Vector-accessed buffers (state, conv_w, out) need 16 bytes; the rest their element size.
+gdn_status_t check_tensors(const gdn_shape_t *s, const gdn_tensors_t *t)
+{
+    if (!t) return GDN_ERR_NULL;
+    const void *req[] = {t->qkv, t->f, t->beta, t->z, t->conv_w, t->A_log, t->dt_bias,
+                         t->norm_w, t->conv_state, t->state, t->out};
+    for (const void *p : req)
+        if (!p) return GDN_ERR_NULL;
+    const unsigned ib = s->in_dtype == GDN_BF16 ? 2u : 4u;
+    if (!aligned(t->qkv, ib) || !aligned(t->f, ib) || !aligned(t->beta, ib) ||
+        !aligned(t->z, ib) || !aligned(t->A_log, 4) || !aligned(t->dt_bias, 4) ||
+        !aligned(t->norm_w, 4) || !aligned(t->conv_state, 4) || !aligned16(t->conv_w) ||
+        !aligned16(t->state) || !aligned16(t->out))
+        return GDN_ERR_ALIGN;
+    return GDN_OK;
+}
+
+gdn::StepArgs step_args(const gdn_shape_t *s, const gdn_tensors_t *t)
+{
+    gdn::StepArgs a = {};
+    a.qkv = t->qkv;
+    a.f = t->f;
+    a.beta = t->beta;
+    a.z = t->z;
+    a.conv_w = t->conv_w;
+    a.A_log = t->A_log;
+    a.dt_bias = t->dt_bias;
+    a.norm_w = t->norm_w;
+    a.state_in = t->state;
+    a.conv_in = t->conv_state;
+    a.out = t->out;
+    a.B = s->B;
+    a.T = s->T;
+    a.H_qk = s->H_qk;
+    a.H_v = s->H_v;
+    a.C = 2 * s->H_qk * s->d_k + s->H_v * s->d_v;
+    a.group = s->H_v / s->H_qk;
+    a.kda = s->gate_mode == GDN_GATE_PER_CHANNEL;
+    a.in_bf16 = s->in_dtype == GDN_BF16;
+    a.out_bf16 = s->out_dtype == GDN_BF16;
+    a.q_scale = s->q_scale;
+    a.eps_l2 = s->eps_l2;
+    a.eps_norm = s->eps_norm;
+    return a;
+}
+
+bool plan_for(const gdn_shape_t *s, gdn::StepPlan *plan)
+{
+    const int sms = num_sms_current();
+    return gdn::plan_step(s->d_k, s->B, s->H_v, s->H_v / s->H_qk, sms > 0 ? sms : 148, plan);
+}
+
+gdn_status_t run_step(const gdn_shape_t *s, const gdn::StepArgs &a, cudaStream_t stream)
+{
+    gdn::StepPlan plan;
+    if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
+    cudaError_t e = gdn::launch_step(plan, a, (s->flags & GDN_FLAG_PDL) != 0, stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_decode_step(const gdn_shape_t *s, const gdn_tensors_t *t, gdn_stream_t stream)
+{
+    gdn_status_t rc = check_shape(s);
+    if (rc != GDN_OK) return rc;
+    if (s->T != 1) return GDN_ERR_SHAPE;
+    rc = check_tensors(s, t);
+    if (rc != GDN_OK) return rc;
+    gdn::StepPlan plan;
+    if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (s->B == 0) return GDN_OK;
+    gdn::StepArgs a = step_args(s, t);
+    a.state_out = t->state;
+    a.conv_out = t->conv_state;
+    return run_step(s, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_verify_T(const gdn_shape_t *s, const gdn_tensors_t *t, gdn_stream_t stream)
+{
+    gdn_status_t rc = check_shape(s);
+    if (rc != GDN_OK) return rc;
+    if (s->T < 1 || s->T > 4) return GDN_ERR_SHAPE;
+    rc = check_tensors(s, t);
+    if (rc != GDN_OK) return rc;
+    if (!t->state_hist) return GDN_ERR_NULL;
+    if (!aligned16(t->state_hist) || (t->conv_hist && !aligned(t->conv_hist, 4)))
+        return GDN_ERR_ALIGN;
+    gdn::StepPlan plan;
+    if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (s->B == 0) return GDN_OK;
+    gdn::StepArgs a = step_args(s, t);
+    a.state_hist = t->state_hist;
+    a.conv_hist = t->conv_hist;
+    return run_step(s, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_shape_t *s)
+{
+    if (check_shape(s) != GDN_OK || s->T < 1) return 0;
+    return gdn::prefill_workspace_bytes(*s);
+}
+
+gdn_status_t gdn_prefill_chunked(const gdn_shape_t *s, const gdn_tensors_t *t, void *workspace,
+                                 size_t workspace_bytes, gdn_stream_t stream)
+{
+    gdn_status_t rc = check_shape(s);
+    if (rc != GDN_OK) return rc;
+    if (s->T < 1) return GDN_ERR_SHAPE;
+    rc = check_tensors(s, t);
+    if (rc != GDN_OK) return rc;
+    if (s->chunk <= 0) return GDN_ERR_SHAPE;
+    const size_t need = gdn::prefill_workspace_bytes(*s);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return GDN_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return GDN_ERR_ALIGN;
+    if (s->B == 0) return GDN_OK;
+    gdn::StepArgs a = step_args(s, t);
+    a.state_out = t->state;
+    a.conv_out = t->conv_state;
+    const int sms = num_sms_current();
+    return gdn::run_prefill(*s, a, workspace, sms > 0 ? sms : 148,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *gdn_status_string(gdn_status_t status)
+{
+    switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_NULL: return "GDN_ERR_NULL: a required pointer is NULL";
+    case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: a pointer is misaligned";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE: invalid sizes";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: no kernel instance for these sizes";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: the CUDA runtime refused a launch";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "unknown gdn_status_t";
+}
+
+const char *gdn_kernel_variant(const gdn_shape_t *s, int op)
+{
+    if (check_shape(s) != GDN_OK) return nullptr;
+    if (op == 2) return gdn::prefill_variant(*s, num_sms_current());
+    gdn::StepPlan plan;
+    if ((op != 0 && op != 1) || !plan_for(s, &plan)) return nullptr;
+    return plan.name;
+}
+
+}  // extern "C"

@@ -1,0 +1,488 @@
+// Recurrent KDA / Gated DeltaNet step on sm_103a: decode (T = 1), verify (T <= 4,
+// per-token states) and in-place multi-token runs, in one kernel template.
+//
+// One CTA owns a column slab of W value columns of one (sequence, value head)
+// state [D, D] (fp32, row = key channel).  The delta rule reduces over key
+// rows inside a column ("llama.cpp PR #84": one state column per warp in the
+// recurrent kernel), so a CTA that holds every key row of its columns needs no
+// other CTA for the update; only the gated RMSNorm needs the whole head, and
+// the D / W slabs of a head exchange one partial sum of squares through
+// distributed shared memory inside a thread-block cluster.
+//
+// Per CTA and token:
+//   1. each thread streams its R rows x 4 columns of the state into registers
+//      (128-bit loads, issued first so they overlap everything below);
+//   2. conv window (K = 4) + SiLU for the head's q and k channels and the
+//      slab's v channels, L2 norms, per-channel or per-head decay, beta;
+//   3. St = Diag(alpha) S in registers, with both column reductions St^T k and
+//      St^T q in the same pass (warp shuffles, then one shared-memory round);
+//   4. u = beta (v - St^T k); o = St^T q + (k.q) u  (= S_new^T q);
+//      S_new = St + k u^T, stored with 128-bit streaming stores;
+//   5. y = o / rms(o) * w * silu(z) over the head's D columns.
+// The state stays in registers across the T tokens of a verify, so verify and
+// T decode calls run the same arithmetic per token.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+__device__ __forceinline__ float ld_in(const void *p, size_t i, int bf16)
+{
+    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+    return reinterpret_cast<const float *>(p)[i];
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float softplus_f(float x)
+{
+    return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+
+// Programmatic dependent launch (no-ops when the launch did not ask for it).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Thread-block cluster helpers.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dsmem_store(float *local, uint32_t rank, float v)
+{
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float conv4(const float4 w, const float *win, float x)
+{
+    float acc = w.x * win[0];
+    acc = fmaf(w.y, win[1], acc);
+    acc = fmaf(w.z, win[2], acc);
+    acc = fmaf(w.w, x, acc);
+    return silu_f(acc);
+}
+
+__device__ __forceinline__ void store_out4(void *out, size_t idx, int bf16, float a, float b,
+                                           float c, float d)
+{
+    if (bf16) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + idx) = pk;
+    } else {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + idx) =
+            make_float4(a, b, c, d);
+    }
+}
+
+constexpr int KM1 = 3;  // conv window rows kept between calls (conv_K - 1)
+
+template <int D, int W, int NT>
+__global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
+{
+    constexpr int TPR = W / 4;          // threads per state row, one float4 each
+    constexpr int RG = NT / TPR;        // row groups
+    constexpr int R = D / RG;           // rows per thread
+    constexpr int NWARP = NT / 32;
+    constexpr int NSLAB = D / W;
+    constexpr int CQ = (D + NT - 1) / NT;  // q/k channel pairs per thread
+    constexpr int CV = (W + NT - 1) / NT;  // v channels per thread
+    static_assert(W % 4 == 0 && 32 % TPR == 0 && NT % 32 == 0 && RG * R == D, "tiling");
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid % TPR, rg = tid / TPR;
+    const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hq = h / a.group;
+    const bool clustered = NSLAB * a.group > 1;
+    const bool qk_owner = (slab == 0) && (h % a.group == 0);  // writes shared q/k conv rows
+    const int C = a.C;
+
+    __shared__ float q_s[D], k_s[D], a_s[D], v_s[W];
+    __shared__ float red3[NWARP][3];
+    __shared__ __align__(16) float red_k[NWARP][W];
+    __shared__ __align__(16) float red_q[NWARP][W];
+    __shared__ float rms_slot[2][NSLAB];
+    __shared__ float beta_s;
+
+    pdl_launch_dependents();
+    uint32_t rank0 = 0;  // cluster rank of slab 0 of this head
+    if (clustered) {
+        rank0 = cluster_rank() - slab;
+        cluster_arrive_relaxed();
+    }
+
+    // 1. state slab -> registers
+    const size_t head = static_cast<size_t>(b) * a.H_v + h;
+    const size_t col0 = static_cast<size_t>(slab) * W + 4 * cg;
+    float4 st[R];
+    {
+        const float *S = a.state_in + head * D * D + col0;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            st[r] = __ldcs(reinterpret_cast<const float4 *>(S + static_cast<size_t>(rg + RG * r) * D));
+    }
+
+    // conv windows and weights of the channels this thread convolves
+    const int tv = (tid + NT - (D % NT)) % NT;  // spreads v channels over idle threads
+    float wq[CQ][KM1], wk[CQ][KM1], wv[CV][KM1];
+    float4 cwq[CQ], cwk[CQ], cwv[CV];
+    float dtb[CQ];
+    const float A = expf(a.A_log[h]);
+#pragma unroll
+    for (int m = 0; m < CQ; ++m) {
+        const int i = tid + m * NT;
+        if (i < D) {
+            const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
+#pragma unroll
+            for (int r = 0; r < KM1; ++r) {
+                wq[m][r] = a.conv_in[(static_cast<size_t>(b) * KM1 + r) * C + cq];
+                wk[m][r] = a.conv_in[(static_cast<size_t>(b) * KM1 + r) * C + ck];
+            }
+            cwq[m] = reinterpret_cast<const float4 *>(a.conv_w)[cq];
+            cwk[m] = reinterpret_cast<const float4 *>(a.conv_w)[ck];
+            dtb[m] = a.kda ? a.dt_bias[static_cast<size_t>(h) * D + i] : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < CV; ++m) {
+        const int j = tv + m * NT;
+        if (j < W) {
+            const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
+#pragma unroll
+            for (int r = 0; r < KM1; ++r)
+                wv[m][r] = a.conv_in[(static_cast<size_t>(b) * KM1 + r) * C + cv];
+            cwv[m] = reinterpret_cast<const float4 *>(a.conv_w)[cv];
+        }
+    }
+    float nw[4] = {0.f, 0.f, 0.f, 0.f};
+    if (rg == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) nw[c] = a.norm_w[col0 + c];
+    }
+    const float dtb_head = a.kda ? 0.0f : a.dt_bias[h];
+
+    // inputs below may come from the previous kernel on the stream
+    pdl_wait();
+
+    for (int t = 0; t < a.T; ++t) {
+        if (t > 0) __syncthreads();  // previous token's shared-memory reads are done
+        const size_t bt = static_cast<size_t>(b) * a.T + t;
+        const size_t in_row = bt * C;
+        const size_t bth = bt * a.H_v + h;
+
+        // 2. conv + SiLU, norms' partial sums, gates
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+        for (int m = 0; m < CQ; ++m) {
+            const int i = tid + m * NT;
+            if (i < D) {
+                const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
+                const float xq = ld_in(a.qkv, in_row + cq, a.in_bf16);
+                const float xk = ld_in(a.qkv, in_row + ck, a.in_bf16);
+                const float q = conv4(cwq[m], wq[m], xq);
+                const float k = conv4(cwk[m], wk[m], xk);
+                wq[m][0] = wq[m][1]; wq[m][1] = wq[m][2]; wq[m][2] = xq;
+                wk[m][0] = wk[m][1]; wk[m][1] = wk[m][2]; wk[m][2] = xk;
+                q_s[i] = q;
+                k_s[i] = k;
+                sq = fmaf(q, q, sq);
+                sk = fmaf(k, k, sk);
+                sqk = fmaf(q, k, sqk);
+                if (a.kda) {
+                    const float fi = ld_in(a.f, bth * D + i, a.in_bf16);
+                    a_s[i] = expf(-A * softplus_f(fi + dtb[m]));
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < CV; ++m) {
+            const int j = tv + m * NT;
+            if (j < W) {
+                const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
+                const float xv = ld_in(a.qkv, in_row + cv, a.in_bf16);
+                v_s[j] = conv4(cwv[m], wv[m], xv);
+                wv[m][0] = wv[m][1]; wv[m][1] = wv[m][2]; wv[m][2] = xv;
+            }
+        }
+        if (tid == 0) {
+            if (!a.kda) a_s[0] = expf(-A * softplus_f(ld_in(a.f, bth, a.in_bf16) + dtb_head));
+            beta_s = sigmoid_f(ld_in(a.beta, bth, a.in_bf16));
+        }
+        // z for the output gate, fetched early
+        float zr[4] = {0.f, 0.f, 0.f, 0.f};
+        if (rg == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) zr[c] = ld_in(a.z, bth * D + col0 + c, a.in_bf16);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+        }
+        if (lane == 0) {
+            red3[warp][0] = sq;
+            red3[warp][1] = sk;
+            red3[warp][2] = sqk;
+        }
+        __syncthreads();
+
+        float Sq = 0.f, Sk = 0.f, Sqk = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) {
+            Sq += red3[w][0];
+            Sk += red3[w][1];
+            Sqk += red3[w][2];
+        }
+        const float rq = a.q_scale / sqrtf(Sq + a.eps_l2);
+        const float rk = 1.0f / sqrtf(Sk + a.eps_l2);
+        const float kq = Sqk * rq * rk;
+        const float beta = beta_s;
+
+        // 3. decay and the two column reductions in one pass
+        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int row = rg + RG * r;
+            const float al = a_s[a.kda ? row : 0];
+            const float kr = k_s[row] * rk, qr = q_s[row] * rq;
+            st[r].x *= al; st[r].y *= al; st[r].z *= al; st[r].w *= al;
+            pk.x = fmaf(st[r].x, kr, pk.x); pk.y = fmaf(st[r].y, kr, pk.y);
+            pk.z = fmaf(st[r].z, kr, pk.z); pk.w = fmaf(st[r].w, kr, pk.w);
+            pq.x = fmaf(st[r].x, qr, pq.x); pq.y = fmaf(st[r].y, qr, pq.y);
+            pq.z = fmaf(st[r].z, qr, pq.z); pq.w = fmaf(st[r].w, qr, pq.w);
+        }
+#pragma unroll
+        for (int off = TPR; off < 32; off <<= 1) {
+            pk.x += __shfl_xor_sync(0xffffffffu, pk.x, off);
+            pk.y += __shfl_xor_sync(0xffffffffu, pk.y, off);
+            pk.z += __shfl_xor_sync(0xffffffffu, pk.z, off);
+            pk.w += __shfl_xor_sync(0xffffffffu, pk.w, off);
+            pq.x += __shfl_xor_sync(0xffffffffu, pq.x, off);
+            pq.y += __shfl_xor_sync(0xffffffffu, pq.y, off);
+            pq.z += __shfl_xor_sync(0xffffffffu, pq.z, off);
+            pq.w += __shfl_xor_sync(0xffffffffu, pq.w, off);
+        }
+        if (lane < TPR) {
+            *reinterpret_cast<float4 *>(&red_k[warp][4 * cg]) = pk;
+            *reinterpret_cast<float4 *>(&red_q[warp][4 * cg]) = pq;
+        }
+        __syncthreads();
+
+        // 4. u, o, state update
+        float kS[4] = {0.f, 0.f, 0.f, 0.f}, qS[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) {
+            const float4 ak = *reinterpret_cast<const float4 *>(&red_k[w][4 * cg]);
+            const float4 aq = *reinterpret_cast<const float4 *>(&red_q[w][4 * cg]);
+            kS[0] += ak.x; kS[1] += ak.y; kS[2] += ak.z; kS[3] += ak.w;
+            qS[0] += aq.x; qS[1] += aq.y; qS[2] += aq.z; qS[3] += aq.w;
+        }
+        float u[4], o[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            u[c] = beta * (v_s[4 * cg + c] - kS[c]);
+            o[c] = fmaf(kq, u[c], qS[c]);
+        }
+        const bool last = (t == a.T - 1);
+        float *hist = a.state_hist
+            ? a.state_hist + ((static_cast<size_t>(t) * a.B + b) * a.H_v + h) * D * D + col0
+            : nullptr;
+        float *commit = (a.state_out && last) ? a.state_out + head * D * D + col0 : nullptr;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int row = rg + RG * r;
+            const float kr = k_s[row] * rk;
+            st[r].x = fmaf(kr, u[0], st[r].x);
+            st[r].y = fmaf(kr, u[1], st[r].y);
+            st[r].z = fmaf(kr, u[2], st[r].z);
+            st[r].w = fmaf(kr, u[3], st[r].w);
+            const size_t off = static_cast<size_t>(row) * D;
+            if (hist) __stcs(reinterpret_cast<float4 *>(hist + off), st[r]);
+            if (commit) __stcs(reinterpret_cast<float4 *>(commit + off), st[r]);
+        }
+
+        // conv history after this token (verify)
+        if (a.conv_hist) {
+            float *ch = a.conv_hist + (static_cast<size_t>(t) * a.B + b) * KM1 * C;
+#pragma unroll
+            for (int m = 0; m < CQ; ++m) {
+                const int i = tid + m * NT;
+                if (i < D && qk_owner) {
+                    const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
+#pragma unroll
+                    for (int r = 0; r < KM1; ++r) {
+                        ch[static_cast<size_t>(r) * C + cq] = wq[m][r];
+                        ch[static_cast<size_t>(r) * C + ck] = wk[m][r];
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < CV; ++m) {
+                const int j = tv + m * NT;
+                if (j < W) {
+                    const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
+#pragma unroll
+                    for (int r = 0; r < KM1; ++r) ch[static_cast<size_t>(r) * C + cv] = wv[m][r];
+                }
+            }
+        }
+
+        // 5. gated RMSNorm over the head's D columns
+        float p = 0.f;
+        if (warp == 0) {
+            if (rg == 0) p = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        }
+        float total = p;
+        if (clustered) {
+            if (t == 0) cluster_wait_acquire();  // every CTA of the cluster has started
+            if (tid == 0) {
+#pragma unroll
+                for (int s = 0; s < NSLAB; ++s) dsmem_store(&rms_slot[t & 1][slab], rank0 + s, p);
+            }
+            cluster_arrive_release();
+            cluster_wait_acquire();
+            total = 0.f;
+#pragma unroll
+            for (int s = 0; s < NSLAB; ++s) total += rms_slot[t & 1][s];
+        }
+        if (rg == 0) {
+            const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
+            float y[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) y[c] = o[c] * rinv * nw[c] * silu_f(zr[c]);
+            store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
+        }
+    }
+
+    // final conv window (commit)
+    if (a.conv_out) {
+        float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
+#pragma unroll
+        for (int m = 0; m < CQ; ++m) {
+            const int i = tid + m * NT;
+            if (i < D && qk_owner) {
+                const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
+#pragma unroll
+                for (int r = 0; r < KM1; ++r) {
+                    co[static_cast<size_t>(r) * C + cq] = wq[m][r];
+                    co[static_cast<size_t>(r) * C + ck] = wk[m][r];
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < CV; ++m) {
+            const int j = tv + m * NT;
+            if (j < W) {
+                const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
+#pragma unroll
+                for (int r = 0; r < KM1; ++r) co[static_cast<size_t>(r) * C + cv] = wv[m][r];
+            }
+        }
+    }
+}
+
+struct Variant {
+    int D, W, NT;
+    void (*fn)(StepArgs);
+    const char *name;
+};
+
+#define GDN_VARIANT(D, W, NT) {D, W, NT, step_kernel<D, W, NT>, "step<" #D "," #W ">"}
+const Variant kVariants[] = {
+    GDN_VARIANT(128, 128, 256), GDN_VARIANT(128, 64, 256), GDN_VARIANT(128, 32, 128),
+    GDN_VARIANT(128, 16, 64),   GDN_VARIANT(64, 64, 128),  GDN_VARIANT(64, 32, 64),
+    GDN_VARIANT(64, 16, 32),    GDN_VARIANT(32, 32, 64),   GDN_VARIANT(32, 16, 32),
+    GDN_VARIANT(16, 16, 32),
+};
+#undef GDN_VARIANT
+
+const Variant *find_variant(int D, int W)
+{
+    for (const Variant &v : kVariants)
+        if (v.D == D && v.W == W) return &v;
+    return nullptr;
+}
+
+}  // namespace
+
+bool plan_step(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
+{
+    if (D != 16 && D != 32 && D != 64 && D != 128) return false;
+    const long units = static_cast<long>(B) * H_v;
+    // Fewest slabs that give every SM two CTAs, within an 8-CTA cluster and W >= 16.
+    int best = 0;
+    for (int nslab = 1; nslab <= 8; nslab *= 2) {
+        const int W = D / nslab;
+        if (W < 16 || nslab * group > 8 || !find_variant(D, W)) break;
+        best = nslab;
+        if (units * nslab >= 2L * num_sms) break;
+    }
+    if (best == 0) return false;
+    const Variant *v = find_variant(D, D / best);
+    plan->D = D;
+    plan->W = v->W;
+    plan->nslab = best;
+    plan->threads = v->NT;
+    plan->cluster = best * group;
+    plan->name = v->name;
+    return true;
+}
+
+cudaError_t launch_step(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
+{
+    const Variant *v = find_variant(plan.D, plan.W);
+    if (!v) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.nslab, a.H_v, a.B);
+    cfg.blockDim = dim3(plan.threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (plan.cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = plan.nslab;
+        attr[n].val.clusterDim.y = a.group;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, v->fn, a);
+}
+
+}  // namespace gdn

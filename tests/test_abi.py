@@ -1,0 +1,143 @@
+"""The C ABI on the host: library loads, exports what include/gdn.h declares,
+and rejects bad arguments before launching anything (no GPU needed: every
+call here fails validation, so no kernel is queued)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_decode_kda_gb300 as gdn
+
+pytestmark = pytest.mark.cpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_decode_kda_gb300 import build
+    build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == sorted(gdn.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _shape(**kw):
+    base = dict(B=2, T=1, H_qk=4, H_v=4, d_k=128, d_v=128, kda=True, bf16_in=True,
+                q_scale=0.08838835)
+    base.update(kw)
+    return gdn.make_shape(**base)
+
+
+def _tensors(addr=0x10000):
+    names = [n for n, _ in gdn.GdnTensors._fields_]
+    return gdn.GdnTensors(**{n: addr + 0x1000 * i for i, n in enumerate(names)})
+
+
+def _call(lib, op, shape, tensors, ws=None, ws_bytes=0):
+    s = ctypes.byref(shape) if shape is not None else None
+    t = ctypes.byref(tensors) if tensors is not None else None
+    if op == "decode":
+        return lib.gdn_decode_step(s, t, None)
+    if op == "verify":
+        return lib.gdn_verify_T(s, t, None)
+    return lib.gdn_prefill_chunked(s, t, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("op", ["decode", "verify", "prefill"])
+def test_null_arguments(lib, op):
+    assert _call(lib, op, None, _tensors()) == gdn.GDN_ERR_NULL
+    assert _call(lib, op, _shape(), None) == gdn.GDN_ERR_NULL
+    t = _tensors()
+    t.qkv = None
+    assert _call(lib, op, _shape(), t) == gdn.GDN_ERR_NULL
+
+
+@pytest.mark.parametrize("op", ["decode", "verify", "prefill"])
+def test_misaligned_pointer(lib, op):
+    t = _tensors()
+    t.state = t.state + 4
+    assert _call(lib, op, _shape(), t) == gdn.GDN_ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(B=-1), gdn.GDN_ERR_SHAPE), (dict(H_qk=3, H_v=4), gdn.GDN_ERR_SHAPE),
+    (dict(H_qk=0), gdn.GDN_ERR_SHAPE), (dict(d_k=128, d_v=64), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(d_k=48, d_v=48), gdn.GDN_ERR_UNSUPPORTED), (dict(conv_K=3), gdn.GDN_ERR_UNSUPPORTED),
+    (dict(q_scale=0.0), gdn.GDN_ERR_SHAPE), (dict(B=70000), gdn.GDN_ERR_SHAPE),
+])
+def test_bad_shapes(lib, kw, want):
+    assert _call(lib, "decode", _shape(**kw), _tensors()) == want
+
+
+def test_bad_enums_and_flags(lib):
+    for field, val in (("gate_mode", 7), ("in_dtype", 3), ("out_dtype", -1), ("flags", 8)):
+        s = _shape()
+        setattr(s, field, val)
+        assert _call(lib, "decode", s, _tensors()) == gdn.GDN_ERR_SHAPE, field
+
+
+def test_token_counts(lib):
+    assert _call(lib, "decode", _shape(T=2), _tensors()) == gdn.GDN_ERR_SHAPE
+    assert _call(lib, "verify", _shape(T=5), _tensors()) == gdn.GDN_ERR_SHAPE
+    assert _call(lib, "verify", _shape(T=0), _tensors()) == gdn.GDN_ERR_SHAPE
+    assert _call(lib, "prefill", _shape(T=0), _tensors()) == gdn.GDN_ERR_SHAPE
+    t = _tensors()
+    t.state_hist = None
+    assert _call(lib, "verify", _shape(T=2), t) == gdn.GDN_ERR_NULL
+
+
+def test_prefill_workspace_checks(lib):
+    s = _shape(T=256, kda=False)
+    need = gdn.gdn_prefill_workspace_bytes(s)
+    assert need >= 0
+    if need > 0:
+        assert _call(lib, "prefill", s, _tensors(), None, need) == gdn.GDN_ERR_WORKSPACE
+        assert _call(lib, "prefill", s, _tensors(), 0x100000, need - 1) == gdn.GDN_ERR_WORKSPACE
+    s.chunk = 0
+    assert _call(lib, "prefill", s, _tensors(), 0x100000, need) == gdn.GDN_ERR_SHAPE
+    bad = _shape(T=0)
+    assert gdn.gdn_prefill_workspace_bytes(bad) == 0
+
+
+def test_status_strings(lib):
+    for code in range(-7, 1):
+        assert gdn.status_string(code).startswith("GDN_")
+    assert "unknown" in gdn.status_string(-99)
+
+
+def test_variant_choice(lib):
+    # B*H_v head units: enough for two CTAs per SM -> whole-head CTAs; B=1 -> 16-column slabs
+    assert gdn.gdn_kernel_variant(_shape(B=64, H_qk=32, H_v=32), gdn.OP_DECODE) == "step<128,128>"
+    assert gdn.gdn_kernel_variant(_shape(B=1, H_qk=32, H_v=32), gdn.OP_DECODE) == "step<128,16>"
+    assert gdn.gdn_kernel_variant(_shape(d_k=16, d_v=16), gdn.OP_DECODE) == "step<16,16>"
+    assert gdn.gdn_kernel_variant(_shape(d_k=48, d_v=48), gdn.OP_DECODE) is None
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package and its CUDA sources import / include nothing from oracle/."""
+    pkg = os.path.join(ROOT, "linear_attention_decode_kda_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".h", ".cuh")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
+                assert "gdn_oracle" not in text, fn
+    src = open(os.path.join(ROOT, "oracle", "gdn_oracle.c")).read()
+    assert not re.search(r'#include\s+"', src), "oracle includes a local header"
