@@ -57,7 +57,7 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = -4, /* valid, but no kernel instance for these sizes    */
     GDN_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required       */
     GDN_ERR_CUDA = -6,        /* the CUDA runtime refused a launch                */
-    GDN_ERR_TIMEOUT = -7      /* reserved: a bounded device wait gave up          */
+    GDN_ERR_TIMEOUT = -7      /* a bounded device wait gave up (gdn_device_status) */
 } gdn_status_t;
 
 typedef enum {
@@ -152,6 +152,16 @@ GDN_API gdn_status_t gdn_prefill_chunked(const gdn_shape_t *shape, const gdn_ten
 
 /* Bytes of device workspace gdn_prefill_chunked needs for this shape (0 on a bad shape). */
 GDN_API size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
+
+/*
+ * Reads and clears the library's device error word on the current device.
+ * Kernels that wait on an mbarrier give up after about two seconds instead of
+ * hanging and record the time-out there; their outputs are then invalid.
+ * Returns GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if the word could not be
+ * read.  Synchronises with the current device (a debugging aid, not for the
+ * hot path).
+ */
+GDN_API gdn_status_t gdn_device_status(void);
 
 /* Static, NUL-terminated name of a status code. */
 GDN_API const char *gdn_status_string(gdn_status_t status);

@@ -53,7 +53,8 @@ class GdnError(RuntimeError):
 
 
 EXPORTS = ("gdn_decode_step", "gdn_verify_T", "gdn_prefill_chunked",
-           "gdn_prefill_workspace_bytes", "gdn_status_string", "gdn_kernel_variant")
+           "gdn_prefill_workspace_bytes", "gdn_device_status", "gdn_status_string",
+           "gdn_kernel_variant")
 
 _lib = None
 
@@ -83,6 +84,8 @@ def load():
     lib.gdn_prefill_workspace_bytes.argtypes = [S]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_device_status.restype = ctypes.c_int
+    lib.gdn_device_status.argtypes = []
     lib.gdn_kernel_variant.restype = ctypes.c_char_p
     lib.gdn_kernel_variant.argtypes = [S, ctypes.c_int]
     _lib = lib
@@ -117,6 +120,11 @@ def gdn_prefill_chunked(shape: GdnShape, tensors: GdnTensors, workspace: int = 0
 
 def gdn_prefill_workspace_bytes(shape: GdnShape) -> int:
     return int(load().gdn_prefill_workspace_bytes(ctypes.byref(shape)))
+
+
+def gdn_device_status() -> None:
+    """Raises GdnError if a kernel recorded a bounded-wait time-out (synchronises)."""
+    _check(load().gdn_device_status(), "gdn_device_status")
 
 
 def gdn_kernel_variant(shape: GdnShape, op: int) -> Optional[str]:

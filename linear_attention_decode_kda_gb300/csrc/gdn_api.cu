@@ -109,7 +109,9 @@ gdn_status_t run_step(const gdn_shape_t *s, const gdn::StepArgs &a, cudaStream_t
 {
     gdn::StepPlan plan;
     if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
-    cudaError_t e = gdn::launch_step(plan, a, (s->flags & GDN_FLAG_PDL) != 0, stream);
+    const int sms = num_sms_current();
+    cudaError_t e = gdn::launch_step(plan, a, (s->flags & GDN_FLAG_PDL) != 0, sms > 0 ? sms : 148,
+                                     stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
@@ -192,6 +194,13 @@ const char *gdn_status_string(gdn_status_t status)
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
     }
     return "unknown gdn_status_t";
+}
+
+gdn_status_t gdn_device_status(void)
+{
+    const unsigned int e = gdn::take_stream_error();
+    if (e == ~0u) return GDN_ERR_CUDA;
+    return e ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 const char *gdn_kernel_variant(const gdn_shape_t *s, int op)

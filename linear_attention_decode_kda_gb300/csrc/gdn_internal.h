@@ -24,16 +24,48 @@ struct StepArgs {
     float q_scale, eps_l2, eps_norm;
 };
 
-// One launch configuration of the step kernel.
+// One launch configuration of the step kernels.
 struct StepPlan {
-    int D = 0, W = 0, nslab = 0, threads = 0, cluster = 1;
+    enum Kind { kSlab, kStream } kind = kSlab;
+    int D = 0, W = 0, nslab = 0, threads = 0, cluster = 1, grid = 0;
     const char *name = nullptr;
 };
 
-// Chooses the column-slab width for B*H_v head units on a GPU with `num_sms` SMs.
-bool plan_step(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
+// Column-slab kernel (gdn_step.cu): any unit count, d in {16, 32, 64, 128}.
+bool plan_slab(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
+cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
 
-// Queues the step kernel.  pdl: programmatic dependent launch attribute.
-cudaError_t launch_step(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
+// Persistent TMA-pipelined kernel (gdn_stream.cu): d = 128, ungrouped heads,
+// at least two (sequence, head) units per SM.
+bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
+// True when every buffer meets the streaming kernel's 16-byte chunk rules.
+bool stream_eligible(const StepArgs &a);
+cudaError_t launch_stream(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
+
+// Reads and clears the streaming kernel's device error word (synchronous).
+unsigned int take_stream_error();
+
+// The plan for B*H_v units on a GPU with `num_sms` SMs.  Decode and verify of
+// the same (B, H_v) always get the same plan, so their per-token arithmetic
+// is identical.
+inline bool plan_step(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
+{
+    return plan_stream(D, B, H_v, group, num_sms, plan) ||
+           plan_slab(D, B, H_v, group, num_sms, plan);
+}
+
+// Queues the planned kernel; a streaming plan whose buffers miss the 16-byte
+// chunk rules runs on the column-slab kernel instead.
+inline cudaError_t launch_step(const StepPlan &plan, const StepArgs &a, bool pdl, int num_sms,
+                               cudaStream_t stream)
+{
+    if (plan.kind == StepPlan::kStream) {
+        if (stream_eligible(a)) return launch_stream(plan, a, pdl, stream);
+        StepPlan slab;
+        if (!plan_slab(plan.D, a.B, a.H_v, a.group, num_sms, &slab)) return cudaErrorInvalidValue;
+        return launch_slab(slab, a, pdl, stream);
+    }
+    return launch_slab(plan, a, pdl, stream);
+}
 
 }  // namespace gdn

@@ -20,7 +20,7 @@ gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *, int nu
 {
     StepPlan plan;
     if (!plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan)) return GDN_ERR_UNSUPPORTED;
-    cudaError_t e = launch_step(plan, a, (s.flags & GDN_FLAG_PDL) != 0, stream);
+    cudaError_t e = launch_step(plan, a, (s.flags & GDN_FLAG_PDL) != 0, num_sms, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

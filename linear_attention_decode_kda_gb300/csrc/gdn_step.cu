@@ -1,5 +1,7 @@
-// Recurrent KDA / Gated DeltaNet step on sm_103a: decode (T = 1), verify (T <= 4,
-// per-token states) and in-place multi-token runs, in one kernel template.
+// Recurrent KDA / Gated DeltaNet step on sm_103a, column-slab form: decode
+// (T = 1), verify (T <= 4, per-token states) and in-place multi-token runs.
+// Used when there are too few (sequence, head) units to fill the GPU with
+// whole heads (single-sequence decode) and for grouped heads.
 //
 // One CTA owns a column slab of W value columns of one (sequence, value head)
 // state [D, D] (fp32, row = key channel).  The delta rule reduces over key
@@ -9,102 +11,41 @@
 // the D / W slabs of a head exchange one partial sum of squares through
 // distributed shared memory inside a thread-block cluster.
 //
-// Per CTA and token:
-//   1. each thread streams its R rows x 4 columns of the state into registers
-//      (128-bit loads, issued first so they overlap everything below);
-//   2. conv window (K = 4) + SiLU for the head's q and k channels and the
-//      slab's v channels, L2 norms, per-channel or per-head decay, beta;
-//   3. St = Diag(alpha) S in registers, with both column reductions St^T k and
-//      St^T q in the same pass (warp shuffles, then one shared-memory round);
-//   4. u = beta (v - St^T k); o = St^T q + (k.q) u  (= S_new^T q);
-//      S_new = St + k u^T, stored with 128-bit streaming stores;
-//   5. y = o / rms(o) * w * silu(z) over the head's D columns.
+// Per CTA:
+//   before the dependency wait (programmatic dependent launch): the state slab
+//   (128-bit loads into registers), the conv windows, conv weights and gate
+//   parameters -- nothing a preceding kernel on the stream writes;
+//   after it, per token, with the next token's inputs already in flight:
+//   1. conv window (K = 4) + SiLU for the head's q and k channels and the
+//      slab's v channels, L2-norm partial sums, per-channel or per-head decay,
+//      beta;
+//   2. St = Diag(alpha) S in registers with both column reductions St^T k and
+//      St^T q in one pass (warp shuffles, then one shared-memory round);
+//   3. u = beta (v - St^T k); o = St^T q + (k.q) u  (= S_new^T q);
+//   4. gated RMSNorm over the head's D columns (cluster exchange happens
+//      before any global store, so its release fence has nothing to drain);
+//   5. S_new = St + k u^T stored with 128-bit streaming stores.
 // The state stays in registers across the T tokens of a verify, so verify and
 // T decode calls run the same arithmetic per token.
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <stdint.h>
-
+#include "gdn_device.cuh"
 #include "gdn_internal.h"
 
 namespace gdn {
 namespace {
 
-__device__ __forceinline__ float ld_in(const void *p, size_t i, int bf16)
-{
-    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
-    return reinterpret_cast<const float *>(p)[i];
-}
-
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
-__device__ __forceinline__ float softplus_f(float x)
-{
-    return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
-}
-
-// Programmatic dependent launch (no-ops when the launch did not ask for it).
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Thread-block cluster helpers.
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void dsmem_store(float *local, uint32_t rank, float v)
-{
-    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ float conv4(const float4 w, const float *win, float x)
-{
-    float acc = w.x * win[0];
-    acc = fmaf(w.y, win[1], acc);
-    acc = fmaf(w.z, win[2], acc);
-    acc = fmaf(w.w, x, acc);
-    return silu_f(acc);
-}
-
-__device__ __forceinline__ void store_out4(void *out, size_t idx, int bf16, float a, float b,
-                                           float c, float d)
-{
-    if (bf16) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + idx) = pk;
-    } else {
-        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + idx) =
-            make_float4(a, b, c, d);
-    }
-}
+using namespace dev;
 
 constexpr int KM1 = 3;  // conv window rows kept between calls (conv_K - 1)
 
+template <int CQ, int CV>
+struct TokenIn {
+    float xq[CQ], xk[CQ], fq[CQ], xv[CV];
+    float z[4];
+    float beta, fh;
+};
+
 template <int D, int W, int NT>
-__global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
+__global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kernel(const StepArgs a)
 {
     constexpr int TPR = W / 4;          // threads per state row, one float4 each
     constexpr int RG = NT / TPR;        // row groups
@@ -122,6 +63,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
     const bool clustered = NSLAB * a.group > 1;
     const bool qk_owner = (slab == 0) && (h % a.group == 0);  // writes shared q/k conv rows
     const int C = a.C;
+    const int tv = (tid + NT - (D % NT)) % NT;  // spreads v channels over idle threads
 
     __shared__ float q_s[D], k_s[D], a_s[D], v_s[W];
     __shared__ float red3[NWARP][3];
@@ -137,7 +79,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
         cluster_arrive_relaxed();
     }
 
-    // 1. state slab -> registers
+    // ---- before the dependency wait: state slab, conv windows, parameters
     const size_t head = static_cast<size_t>(b) * a.H_v + h;
     const size_t col0 = static_cast<size_t>(slab) * W + 4 * cg;
     float4 st[R];
@@ -147,9 +89,6 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
         for (int r = 0; r < R; ++r)
             st[r] = __ldcs(reinterpret_cast<const float4 *>(S + static_cast<size_t>(rg + RG * r) * D));
     }
-
-    // conv windows and weights of the channels this thread convolves
-    const int tv = (tid + NT - (D % NT)) % NT;  // spreads v channels over idle threads
     float wq[CQ][KM1], wk[CQ][KM1], wv[CV][KM1];
     float4 cwq[CQ], cwk[CQ], cwv[CV];
     float dtb[CQ];
@@ -187,58 +126,77 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
     }
     const float dtb_head = a.kda ? 0.0f : a.dt_bias[h];
 
-    // inputs below may come from the previous kernel on the stream
+    // ---- inputs may be written by the previous kernel on the stream
     pdl_wait();
 
+    // All inputs of token t in one round of independent loads.
+    auto load_token = [&](int t, TokenIn<CQ, CV> &in) {
+        const size_t bt = static_cast<size_t>(b) * a.T + t;
+        const size_t row = bt * C;
+        const size_t bth = bt * a.H_v + h;
+#pragma unroll
+        for (int m = 0; m < CQ; ++m) {
+            const int i = tid + m * NT;
+            if (i < D) {
+                in.xq[m] = ld_in(a.qkv, row + hq * D + i, a.in_bf16);
+                in.xk[m] = ld_in(a.qkv, row + a.H_qk * D + hq * D + i, a.in_bf16);
+                in.fq[m] = a.kda ? ld_in(a.f, bth * D + i, a.in_bf16) : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < CV; ++m) {
+            const int j = tv + m * NT;
+            if (j < W) in.xv[m] = ld_in(a.qkv, row + 2 * a.H_qk * D + h * D + slab * W + j, a.in_bf16);
+        }
+        if (rg == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) in.z[c] = ld_in(a.z, bth * D + col0 + c, a.in_bf16);
+        }
+        if (tid == 0) {
+            in.beta = ld_in(a.beta, bth, a.in_bf16);
+            in.fh = a.kda ? 0.0f : ld_in(a.f, bth, a.in_bf16);
+        }
+    };
+
+    TokenIn<CQ, CV> cur;
+    load_token(0, cur);
+
+#pragma unroll 1
     for (int t = 0; t < a.T; ++t) {
         if (t > 0) __syncthreads();  // previous token's shared-memory reads are done
-        const size_t bt = static_cast<size_t>(b) * a.T + t;
-        const size_t in_row = bt * C;
-        const size_t bth = bt * a.H_v + h;
+        TokenIn<CQ, CV> nxt;
+        if (t + 1 < a.T) load_token(t + 1, nxt);
+        const size_t bth = (static_cast<size_t>(b) * a.T + t) * a.H_v + h;
 
-        // 2. conv + SiLU, norms' partial sums, gates
+        // 1. conv + SiLU, norms' partial sums, gates
         float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
         for (int m = 0; m < CQ; ++m) {
             const int i = tid + m * NT;
             if (i < D) {
-                const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
-                const float xq = ld_in(a.qkv, in_row + cq, a.in_bf16);
-                const float xk = ld_in(a.qkv, in_row + ck, a.in_bf16);
-                const float q = conv4(cwq[m], wq[m], xq);
-                const float k = conv4(cwk[m], wk[m], xk);
-                wq[m][0] = wq[m][1]; wq[m][1] = wq[m][2]; wq[m][2] = xq;
-                wk[m][0] = wk[m][1]; wk[m][1] = wk[m][2]; wk[m][2] = xk;
+                const float q = conv4_silu(cwq[m], wq[m], cur.xq[m]);
+                const float k = conv4_silu(cwk[m], wk[m], cur.xk[m]);
+                wq[m][0] = wq[m][1]; wq[m][1] = wq[m][2]; wq[m][2] = cur.xq[m];
+                wk[m][0] = wk[m][1]; wk[m][1] = wk[m][2]; wk[m][2] = cur.xk[m];
                 q_s[i] = q;
                 k_s[i] = k;
                 sq = fmaf(q, q, sq);
                 sk = fmaf(k, k, sk);
                 sqk = fmaf(q, k, sqk);
-                if (a.kda) {
-                    const float fi = ld_in(a.f, bth * D + i, a.in_bf16);
-                    a_s[i] = expf(-A * softplus_f(fi + dtb[m]));
-                }
+                if (a.kda) a_s[i] = expf(-A * softplus_f(cur.fq[m] + dtb[m]));
             }
         }
 #pragma unroll
         for (int m = 0; m < CV; ++m) {
             const int j = tv + m * NT;
             if (j < W) {
-                const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
-                const float xv = ld_in(a.qkv, in_row + cv, a.in_bf16);
-                v_s[j] = conv4(cwv[m], wv[m], xv);
-                wv[m][0] = wv[m][1]; wv[m][1] = wv[m][2]; wv[m][2] = xv;
+                v_s[j] = conv4_silu(cwv[m], wv[m], cur.xv[m]);
+                wv[m][0] = wv[m][1]; wv[m][1] = wv[m][2]; wv[m][2] = cur.xv[m];
             }
         }
         if (tid == 0) {
-            if (!a.kda) a_s[0] = expf(-A * softplus_f(ld_in(a.f, bth, a.in_bf16) + dtb_head));
-            beta_s = sigmoid_f(ld_in(a.beta, bth, a.in_bf16));
-        }
-        // z for the output gate, fetched early
-        float zr[4] = {0.f, 0.f, 0.f, 0.f};
-        if (rg == 0) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) zr[c] = ld_in(a.z, bth * D + col0 + c, a.in_bf16);
+            if (!a.kda) a_s[0] = expf(-A * softplus_f(cur.fh + dtb_head));
+            beta_s = sigmoid_f(cur.beta);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -265,7 +223,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
         const float kq = Sqk * rq * rk;
         const float beta = beta_s;
 
-        // 3. decay and the two column reductions in one pass
+        // 2. decay and the two column reductions in one pass
         float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -295,7 +253,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
         }
         __syncthreads();
 
-        // 4. u, o, state update
+        // 3. u and o for this thread's four columns
         float kS[4] = {0.f, 0.f, 0.f, 0.f}, qS[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int w = 0; w < NWARP; ++w) {
@@ -310,6 +268,36 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
             u[c] = beta * (v_s[4 * cg + c] - kS[c]);
             o[c] = fmaf(kq, u[c], qS[c]);
         }
+
+        // 4. gated RMSNorm over the head's D columns
+        float p = 0.f;
+        if (warp == 0) {
+            if (rg == 0) p = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        }
+        float total = p;
+        if (clustered) {
+            if (t == 0) cluster_wait_acquire();  // every CTA of the cluster has started
+            if (tid == 0) {
+#pragma unroll
+                for (int s = 0; s < NSLAB; ++s) dsmem_store(&rms_slot[t & 1][slab], rank0 + s, p);
+            }
+            cluster_arrive_release();
+            cluster_wait_acquire();
+            total = 0.f;
+#pragma unroll
+            for (int s = 0; s < NSLAB; ++s) total += rms_slot[t & 1][s];
+        }
+        if (rg == 0) {
+            const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
+            float y[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) y[c] = o[c] * rinv * nw[c] * silu_f(cur.z[c]);
+            store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
+        }
+
+        // 5. state update and stores
         const bool last = (t == a.T - 1);
         float *hist = a.state_hist
             ? a.state_hist + ((static_cast<size_t>(t) * a.B + b) * a.H_v + h) * D * D + col0
@@ -328,7 +316,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
             if (commit) __stcs(reinterpret_cast<float4 *>(commit + off), st[r]);
         }
 
-        // conv history after this token (verify)
+        // conv window after this token (verify history)
         if (a.conv_hist) {
             float *ch = a.conv_hist + (static_cast<size_t>(t) * a.B + b) * KM1 * C;
 #pragma unroll
@@ -353,37 +341,11 @@ __global__ void __launch_bounds__(NT, 512 / NT) step_kernel(const StepArgs a)
                 }
             }
         }
-
-        // 5. gated RMSNorm over the head's D columns
-        float p = 0.f;
-        if (warp == 0) {
-            if (rg == 0) p = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-        }
-        float total = p;
-        if (clustered) {
-            if (t == 0) cluster_wait_acquire();  // every CTA of the cluster has started
-            if (tid == 0) {
-#pragma unroll
-                for (int s = 0; s < NSLAB; ++s) dsmem_store(&rms_slot[t & 1][slab], rank0 + s, p);
-            }
-            cluster_arrive_release();
-            cluster_wait_acquire();
-            total = 0.f;
-#pragma unroll
-            for (int s = 0; s < NSLAB; ++s) total += rms_slot[t & 1][s];
-        }
-        if (rg == 0) {
-            const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
-            float y[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) y[c] = o[c] * rinv * nw[c] * silu_f(zr[c]);
-            store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
-        }
+        cur = nxt;
     }
 
-    // final conv window (commit)
+    // final conv window (commit); every reader of the shared q/k rows has
+    // passed the last cluster barrier (or is this CTA)
     if (a.conv_out) {
         float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
 #pragma unroll
@@ -434,7 +396,7 @@ const Variant *find_variant(int D, int W)
 
 }  // namespace
 
-bool plan_step(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
+bool plan_slab(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
 {
     if (D != 16 && D != 32 && D != 64 && D != 128) return false;
     const long units = static_cast<long>(B) * H_v;
@@ -448,16 +410,18 @@ bool plan_step(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
     }
     if (best == 0) return false;
     const Variant *v = find_variant(D, D / best);
+    plan->kind = StepPlan::kSlab;
     plan->D = D;
     plan->W = v->W;
     plan->nslab = best;
     plan->threads = v->NT;
     plan->cluster = best * group;
+    plan->grid = static_cast<int>(units) * best;
     plan->name = v->name;
     return true;
 }
 
-cudaError_t launch_step(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
+cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
 {
     const Variant *v = find_variant(plan.D, plan.W);
     if (!v) return cudaErrorInvalidValue;

@@ -205,3 +205,40 @@ def test_prefill_kda_slow_decay():
 
 def test_prefill_gdn_b4_t4096():
     _prefill(synth.WORKLOADS["gdn_prefill_b4_t4096"]["shape"])
+
+
+def test_stream_shape_with_unaligned_scalars_falls_back_and_matches():
+    """A many-head decode whose beta rows are not 16-byte aligned runs on the
+    column-slab kernel (the streaming kernel needs aligned chunks); same result."""
+    shape = synth.Shape(B=16, T=1, H_qk=32, H_v=32, d_k=128, d_v=128, kda=True)
+    params, inp, state = _case(shape, 2)
+    from gpu_harness import steps_major
+    case = dev.upload(shape, params, synth.Inputs(inp.qkv[:, :1], inp.f[:, :1], inp.beta[:, :1],
+                                                  inp.z[:, :1]), state)
+    beta_all = dev.to_torch(steps_major(inp.beta), True, "cuda")      # [2, B, 1, H]
+    pad = torch.empty(beta_all.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    shifted = pad[1:1 + beta_all.numel()].view(beta_all.shape)       # 2-byte offset
+    shifted.copy_(beta_all)
+    qkv = dev.to_torch(steps_major(inp.qkv), True, "cuda")
+    f = dev.to_torch(steps_major(inp.f), True, "cuda")
+    z = dev.to_torch(steps_major(inp.z), True, "cuda")
+    out = torch.empty((2, shape.B, shape.H_v * shape.d_v), device="cuda")
+    sh = case.abi_shape()
+    for t in range(2):
+        tens = gdn.tensors_from_torch(qkv=qkv[t], f=f[t], beta=shifted[t], z=z[t],
+                                      conv_w=case.conv_w, A_log=case.A_log, dt_bias=case.dt_bias,
+                                      norm_w=case.norm_w, conv_state=case.conv_state,
+                                      state=case.state, out=out[t])
+        gdn.gdn_decode_step(sh, tens, stream())
+    torch.cuda.synchronize()
+    gdn.gdn_device_status()
+    ref = oracle_run(shape, params, inp, state)
+    y = out.permute(1, 0, 2).reshape(ref["y"].shape)
+    assert_close(y, ref["y"], DECODE_TOL, "y")
+    assert_close(case.state, ref["state"], DECODE_TOL, "state")
+
+
+def test_device_status_clean_after_streaming_runs():
+    shape = synth.WORKLOADS["kda_decode_b64"]["shape"]
+    _check_decode(shape, 2)
+    gdn.gdn_device_status()
