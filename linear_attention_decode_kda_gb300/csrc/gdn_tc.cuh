@@ -1,0 +1,141 @@
+// tcgen05 (5th-generation tensor core) helpers for sm_100 / sm_103a, inline PTX.
+//
+// Conventions used by every caller:
+//   * cta_group::1, M = 128: row r of the accumulator D lives in TMEM lane r,
+//     fp32 column c in TMEM column (d_col + c).  Warp w of the CTA reaches the
+//     32 lanes 32 * (w % 4) .. 32 * (w % 4) + 31 with tcgen05.ld / st.
+//   * Operands A (M x K) and B (N x K) are bf16, K-major, in the canonical
+//     no-swizzle layout of 8 x 8 "core matrices" (8 rows x 16 bytes, stored as
+//     128 contiguous bytes).  Core matrix (row group g, K group q) of an
+//     operand with `kdim` columns sits at byte ((g * (kdim / 8)) + q) * 128, so
+//     the stride between K groups (leading byte offset) is 128 bytes and the
+//     stride between row groups (stride byte offset) is kdim * 16 bytes.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace gdn {
+namespace tc {
+
+// Byte offset of element (r, k) of a K-major canonical operand with kdim columns.
+__host__ __device__ __forceinline__ uint32_t op_offset(int r, int k, int kdim)
+{
+    return static_cast<uint32_t>((((r >> 3) * (kdim >> 3)) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor (no swizzle) for the K group pair starting at
+// element column k0 of an operand at shared address `base` with kdim columns.
+__device__ __forceinline__ uint64_t op_desc(uint32_t base, int k0, int kdim)
+{
+    const uint32_t start = base + static_cast<uint32_t>(k0 >> 3) * 128;
+    const uint64_t lbo = 128, sbo = static_cast<uint64_t>(kdim) * 16;
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((start & 0x3FFFF) >> 4);   // bits 0-13: start address
+    d |= ((lbo >> 4) & 0x3FFF) << 16;                       // bits 16-29: leading byte offset
+    d |= ((sbo >> 4) & 0x3FFF) << 32;                       // bits 32-45: stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                    // bits 46-48: descriptor version 1
+    return d;                                               // base offset 0, no swizzle
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both K-major.
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool negate_a)
+{
+    uint32_t d = 0;
+    d |= 1u << 4;                                    // D format: fp32
+    d |= 1u << 7;                                    // A format: bf16
+    d |= 1u << 10;                                   // B format: bf16
+    if (negate_a) d |= 1u << 13;                     // negate A
+    d |= static_cast<uint32_t>(N >> 3) << 17;        // N / 8
+    d |= static_cast<uint32_t>(M >> 4) << 24;        // M / 16
+    return d;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// One warp allocates `ncols` TMEM columns; the address lands in *slot (shared).
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem] (+)= A * B^T over one K step of 16; issued by a single thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
+
+// Arrives on the mbarrier when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive fp32 columns: this thread gets columns col .. col+15 of its lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// TMEM address of (lane, column) for the warp's lane quadrant.
+__device__ __forceinline__ uint32_t taddr(uint32_t base, int lane_base, int col)
+{
+    return base + (static_cast<uint32_t>(lane_base) << 16) + static_cast<uint32_t>(col);
+}
+
+}  // namespace tc
+}  // namespace gdn
