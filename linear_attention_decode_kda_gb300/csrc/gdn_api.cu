@@ -198,9 +198,9 @@ const char *gdn_status_string(gdn_status_t status)
 
 gdn_status_t gdn_device_status(void)
 {
-    const unsigned int e = gdn::take_stream_error();
-    if (e == ~0u) return GDN_ERR_CUDA;
-    return e ? GDN_ERR_TIMEOUT : GDN_OK;
+    const unsigned int e = gdn::take_stream_error(), p = gdn::take_prefill_error();
+    if (e == ~0u || p == ~0u) return GDN_ERR_CUDA;
+    return (e | p) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 const char *gdn_kernel_variant(const gdn_shape_t *s, int op)

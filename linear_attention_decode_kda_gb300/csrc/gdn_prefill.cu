@@ -1,14 +1,571 @@
-// Prefill: T tokens per sequence, state and conv window advanced in place.
-// This version runs the tokens through the recurrent step kernel (the state
-// stays in registers across all T tokens).
+// Prefill of T tokens per sequence; state and conv window advanced in place.
+//
+// Gated DeltaNet (one decay per head), d_k = d_v = 128, bf16 inputs: the
+// chunked WY/UT form ("llama.cpp PR #84", chunked KDA prefill; the gate here
+// is per head) on tcgen05 tensor cores.  Other shapes run the T tokens
+// through the recurrent step kernel.
+//
+// Per chunk of C = 64 tokens with start state S0 (G_t = cumulative log-decay
+// inside the chunk, every exponent <= 0):
+//   A[t][s] = beta_t (k_t . k_s) e^{G_t - G_s}   (s < t),   T = (I + A)^-1
+//   W = T (beta e^G k),  U = T (beta v),  V_new = U - W S0
+//   O = (e^G q) S0 + M V_new,   M[t][s] = (q_t . k_s) e^{G_t - G_s}  (s <= t)
+//   S = e^{G_last} S0 + (k e^{G_last - G})^T V_new
+// Operands are fp16 (kind::f16), accumulation fp32.
+// Everything is computed transposed so that every product has M = 128 rows
+// (the head dimension) on the tensor core: S^T (d_v x d_k, fp32) lives in TMEM
+// as an accumulator, V_new^T, O^T, W^T, U^T too.  The q/k L2 norms come from
+// the diagonal of one Gram product [k; q] [k; q]^T whose off-diagonal blocks
+// give k.k and q.k.  The triangular inverse is a blocked forward substitution
+// in fp32 on the CUDA cores.  One CTA (4 warps) owns one (sequence, value
+// head); value heads sharing a qk head form a thread-block cluster so the
+// shared q/k conv rows are written only after every CTA has read them.
+#include "gdn_device.cuh"
 #include "gdn_prefill.h"
+#include "gdn_tc.cuh"
+
+#include <cuda_fp16.h>
 
 namespace gdn {
+namespace {
+
+using namespace dev;
+
+constexpr int PD = 128;   // d_k = d_v
+constexpr int CH = 32;    // chunk length
+constexpr int PT = 128;   // threads (4 warps = the 128 TMEM lanes)
+constexpr int KM1 = 3;
+
+// Dynamic shared memory (bytes).  Regions are reused once their readers are done.
+// Operands marked "split" are stored as fp16 hi and lo halves (x ~ hi + lo).
+constexpr int SM_RAW = 0;                          // [CH][3][PD] bf16 q|k|v rows of the chunk
+constexpr int SM_Z = SM_RAW + CH * 3 * PD * 2;     // [CH][PD] bf16 output-gate rows
+constexpr int SM_ST = SM_Z + CH * PD * 2;          // split S^T [PD x PD]: hi, then lo
+constexpr int SM_R1 = SM_ST + 2 * PD * PD * 2;     // [k; q] hi over [k; q] lo as one 128-row
+                                                   // operand -> W [CH x PD] -> o^2 [PD][CH] f32
+constexpr int SM_R2 = SM_R1 + 2 * 2 * CH * PD * 2; // split (beta v)^T, k_bg^T -> split V_new^T, M
+constexpr int SM_R3 = SM_R2 + 3 * PD * CH * 2;     // split (e^G q), split k_t^T
+constexpr int SM_R4 = SM_R3 + 4 * CH * PD * 2;     // T [CH x CH]
+constexpr int SM_R5 = SM_R4 + CH * CH * 2;         // Gram f32 [2CH][2CH], A f32, T f32
+constexpr int SM_BYTES = SM_R5 + 4 * CH * CH * 4 + 2 * CH * CH * 4;
+// operand offsets inside the regions
+constexpr int OP_VB = 0, OP_KBG = 2 * PD * CH * 2;                  // R2 (first use)
+constexpr int OP_VN = 0, OP_M = 2 * PD * CH * 2;                    // R2 (second use)
+constexpr int OP_QG = 0, OP_KT = 2 * CH * PD * 2;                   // R3
+constexpr int F_GRAM = 0, F_A = 4 * CH * CH * 4, F_T = F_A + CH * CH * 4;  // R5 (bytes)
+
+// TMEM columns.
+constexpr int TM_GRAM = 0;    // 128 columns: [k; q]_{hi;lo} [k; q]_{hi;lo}^T
+constexpr int TM_WT = 128;    // CH: W^T
+constexpr int TM_UT = 160;    // CH: U^T, then V_new^T
+constexpr int TM_OT = 192;    // CH: O^T
+constexpr int TM_ST = 256;    // 128: S^T
+
+__device__ unsigned int g_prefill_error;  // bit 0: a bounded mbarrier wait gave up
+
+struct PrefillShared {
+    float G[CH], eG[CH], beta[CH], rk[CH], rq[CH], rinv[CH], part[4][CH];
+    float Rt[16][16];
+    uint64_t raw_full, z_full, mma_bar;
+    uint32_t tmem;
+};
+
+// Tensor-core operands are fp16 (11 significant bits); the precision-critical
+// ones are kept as hi + lo pairs and multiplied as hi*hi + hi*lo + lo*hi.
+__device__ __forceinline__ void put_h(unsigned char *base, uint32_t off, float v)
+{
+    *reinterpret_cast<__half *>(base + off) = __float2half_rn(v);
+}
+__device__ __forceinline__ void put_split(unsigned char *hi, unsigned char *lo, uint32_t off, float v)
+{
+    const __half h = __float2half_rn(v);
+    *reinterpret_cast<__half *>(hi + off) = h;
+    *reinterpret_cast<__half *>(lo + off) = __float2half_rn(v - __half2float(h));
+}
+__device__ __forceinline__ float get_h(const unsigned char *base, uint32_t off)
+{
+    return __half2float(*reinterpret_cast<const __half *>(base + off));
+}
+__device__ __forceinline__ float get_bf16(const unsigned char *base, uint32_t off)
+{
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
+}
+
+// Makes this thread's shared-memory writes visible to the tensor core, then syncs the CTA.
+__device__ __forceinline__ void publish_smem()
+{
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+}
+
+// D (+)= A B^T over K in steps of 16 (single thread).
+__device__ __forceinline__ void mma_chain(uint32_t d, uint32_t a, uint32_t b, int kdim,
+                                          uint32_t idesc, bool acc)
+{
+    for (int k0 = 0; k0 < kdim; k0 += 16)
+        tc::mma_f16(d, tc::op_desc(a, k0, kdim), tc::op_desc(b, k0, kdim), idesc, acc || k0 > 0);
+}
+
+// D (+)= (A_hi + A_lo)(B_hi + B_lo)^T without the lo*lo term.
+__device__ __forceinline__ void mma_split(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh,
+                                          uint32_t bl, int kdim, uint32_t idesc, bool acc)
+{
+    mma_chain(d, ah, bh, kdim, idesc, acc);
+    mma_chain(d, ah, bl, kdim, idesc, true);
+    mma_chain(d, al, bh, kdim, idesc, true);
+}
+
+__global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ __align__(16) PrefillShared ps;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.y, hq = h / a.group;
+    const int T = a.T, C = a.C, H = a.H_v;
+    const bool clustered = a.group > 1;
+    const bool qk_owner = (h % a.group) == 0;
+    const size_t head = static_cast<size_t>(b) * H + h;
+    const int lb = 32 * warp;  // this warp's TMEM lane quadrant; thread tid <-> lane tid
+    unsigned char *raw = sm + SM_RAW, *zs = sm + SM_Z;
+    unsigned char *st_hi = sm + SM_ST, *st_lo = sm + SM_ST + PD * PD * 2;
+    unsigned char *r1 = sm + SM_R1, *r2 = sm + SM_R2, *r3 = sm + SM_R3, *r4 = sm + SM_R4;
+    float *Gf = reinterpret_cast<float *>(sm + SM_R5 + F_GRAM);   // [2CH][2CH]
+    float *Af = reinterpret_cast<float *>(sm + SM_R5 + F_A);      // [CH][CH]
+    float *Tf = reinterpret_cast<float *>(sm + SM_R5 + F_T);      // [CH][CH]
+    const int chq = hq * PD, chk = a.H_qk * PD + hq * PD, chv = 2 * a.H_qk * PD + h * PD;
+    constexpr int NR = 2 * CH;  // rows of [k; q]; the lo copy follows as rows NR .. 2NR-1
+
+    if (warp == 0) tc::tmem_alloc(&ps.tmem, 512);
+    if (tid == 0) {
+        mbar_init(&ps.raw_full, 1);
+        mbar_init(&ps.z_full, 1);
+        mbar_init(&ps.mma_bar, 1);
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = ps.tmem;
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // parameters and the conv window of channel tid (q, k of qk head hq; v of head h)
+    const float A_h = expf(a.A_log[h]);
+    const float dt_h = a.dt_bias[h];
+    const float nw = a.norm_w[tid];
+    const float4 cwq = reinterpret_cast<const float4 *>(a.conv_w)[chq + tid];
+    const float4 cwk = reinterpret_cast<const float4 *>(a.conv_w)[chk + tid];
+    const float4 cwv = reinterpret_cast<const float4 *>(a.conv_w)[chv + tid];
+    float wq[KM1], wk[KM1], wv[KM1];
+#pragma unroll
+    for (int r = 0; r < KM1; ++r) {
+        const float *row = a.conv_in + (static_cast<size_t>(b) * KM1 + r) * C;
+        wq[r] = row[chq + tid];
+        wk[r] = row[chk + tid];
+        wv[r] = row[chv + tid];
+    }
+    if (clustered) cluster_arrive_relaxed();  // this CTA has read the shared q/k conv rows
+
+    // state: S[i][j] -> TMEM S^T (lane j = tid, column i) and its split operand copy
+    {
+        const float *Sg = a.state_in + head * PD * PD;
+        for (int i0 = 0; i0 < PD; i0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) v[ii] = Sg[(i0 + ii) * PD + tid];
+            tc::tmem_st16(tc::taddr(tm, lb, TM_ST + i0), v);
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) put_split(st_hi, st_lo, tc::op_offset(tid, i0 + ii, PD), v[ii]);
+        }
+    }
+
+    auto issue_raw = [&](int c0) {  // warp 0: q, k, v rows of the chunk at c0
+        const int n = min(CH, T - c0);
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(&ps.raw_full, static_cast<uint32_t>(n) * 3 * PD * 2);
+        }
+        __syncwarp();
+        for (int i = lane; i < 3 * n; i += 32) {
+            const int t = i / 3, sg = i % 3;
+            const int ch = sg == 0 ? chq : (sg == 1 ? chk : chv);
+            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(a.qkv) +
+                                       (static_cast<size_t>(b) * T + c0 + t) * C + ch;
+            tma_load_1d(raw + (t * 3 + sg) * PD * 2, src, PD * 2, &ps.raw_full);
+        }
+    };
+    auto issue_z = [&](int c0) {  // warp 0: output-gate rows of the chunk at c0
+        const int n = min(CH, T - c0);
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(&ps.z_full, static_cast<uint32_t>(n) * PD * 2);
+        }
+        __syncwarp();
+        for (int t = lane; t < n; t += 32) {
+            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(a.z) +
+                                       ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD;
+            tma_load_1d(zs + t * PD * 2, src, PD * 2, &ps.z_full);
+        }
+    };
+    if (warp == 0) {
+        issue_raw(0);
+        issue_z(0);
+    }
+    // gate logits of the next chunk, one token per lane of warp 0
+    float f_nx = 0.f, b_nx = 0.f;
+    if (tid < CH && tid < T) {
+        const size_t e = (static_cast<size_t>(b) * T + tid) * H + h;
+        f_nx = ld_in(a.f, e, 1);
+        b_nx = ld_in(a.beta, e, 1);
+    }
+
+    bool ok = true;
+    uint32_t raw_ph = 0, z_ph = 0, mma_ph = 0;
+    auto mma_wait = [&]() {
+        if (ok) ok = mbar_wait_bounded(&ps.mma_bar, mma_ph);
+        mma_ph ^= 1u;
+        tc::fence_after_sync();
+    };
+
+#pragma unroll 1
+    for (int c0 = 0; c0 < T; c0 += CH) {
+        const int n = min(CH, T - c0);
+
+        // P0: log-decay g, beta; G = inclusive prefix sum of g inside the chunk (warp 0)
+        if (warp == 0) {
+            float g = 0.f, bt = 0.f;
+            if (lane < n) {
+                g = -A_h * softplus_f(f_nx + dt_h);
+                bt = sigmoid_f(b_nx);
+            }
+            if (c0 + CH + lane < T) {  // next chunk's logits, in flight during this one
+                const size_t e = (static_cast<size_t>(b) * T + c0 + CH + lane) * H + h;
+                f_nx = ld_in(a.f, e, 1);
+                b_nx = ld_in(a.beta, e, 1);
+            }
+            float Gt = g;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, Gt, off);
+                if (lane >= off) Gt += y;
+            }
+            ps.G[lane] = Gt;
+            ps.eG[lane] = expf(Gt);
+            ps.beta[lane] = bt;
+        }
+        if (ok) ok = mbar_wait_bounded(&ps.raw_full, raw_ph);
+        raw_ph ^= 1u;
+        __syncthreads();
+
+        // P1: conv + SiLU along the chunk for channel tid; split [k; q] rows and (beta v)^T
+        for (int t = 0; t < CH; ++t) {
+            float q = 0.f, k = 0.f, v = 0.f;
+            if (t < n) {
+                const float xq = get_bf16(raw, (t * 3 + 0) * PD * 2 + tid * 2);
+                const float xk = get_bf16(raw, (t * 3 + 1) * PD * 2 + tid * 2);
+                const float xv = get_bf16(raw, (t * 3 + 2) * PD * 2 + tid * 2);
+                q = conv4_silu(cwq, wq, xq);
+                k = conv4_silu(cwk, wk, xk);
+                v = conv4_silu(cwv, wv, xv);
+                wq[0] = wq[1]; wq[1] = wq[2]; wq[2] = xq;
+                wk[0] = wk[1]; wk[1] = wk[2]; wk[2] = xk;
+                wv[0] = wv[1]; wv[1] = wv[2]; wv[2] = xv;
+            }
+            put_split(r1, r1 + NR * PD * 2, tc::op_offset(t, tid, PD), k);
+            put_split(r1, r1 + NR * PD * 2, tc::op_offset(CH + t, tid, PD), q);
+            put_split(r2 + OP_VB, r2 + OP_VB + PD * CH * 2, tc::op_offset(tid, t, CH), ps.beta[t] * v);
+        }
+        publish_smem();
+        if (warp == 0 && c0 + CH < T) issue_raw(c0 + CH);  // the raw stage is consumed
+
+        // P2: Gram of the 128-row operand [k; q]_hi over [k; q]_lo with itself
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t a1 = tc::smem_u32(r1);
+            mma_chain(tm + TM_GRAM, a1, a1, PD, tc::idesc_f16(128, 2 * NR, false), false);
+            tc::mma_commit(&ps.mma_bar);
+        }
+        mma_wait();
+
+        // P3: exact Gram of [k; q]: hi.hi + hi.lo (rows < NR) + lo.hi (rows >= NR, moved through smem)
+        if (warp >= 2) {
+            for (int s0 = 0; s0 < NR; s0 += 16) {
+                float v[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_GRAM + s0), v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Gf[(tid - NR) * NR + s0 + i] = v[i];
+            }
+        }
+        __syncthreads();
+        if (warp < 2) {
+            for (int s0 = 0; s0 < NR; s0 += 16) {
+                float hh[16], hl[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_GRAM + s0), hh);
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_GRAM + NR + s0), hl);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Gf[tid * NR + s0 + i] += hh[i] + hl[i];
+            }
+        }
+        __syncthreads();
+        if (tid < CH) {
+            ps.rk[tid] = tid < n ? 1.0f / sqrtf(Gf[tid * NR + tid] + a.eps_l2) : 0.f;
+            ps.rq[tid] = tid < n ? a.q_scale / sqrtf(Gf[(CH + tid) * NR + CH + tid] + a.eps_l2) : 0.f;
+        }
+        __syncthreads();
+        for (int e = tid; e < CH * CH; e += PT) {  // A = beta_t rk_t rk_s (k.k) e^{G_t - G_s}, s < t
+            const int t = e / CH, s = e % CH;
+            Af[e] = (s < t && t < n) ? ps.beta[t] * ps.rk[t] * ps.rk[s] * Gf[t * NR + s] * expf(ps.G[t] - ps.G[s]) : 0.f;
+            Tf[e] = 0.f;
+        }
+        __syncthreads();
+
+        // P4: T = (I + A)^-1: two 16 x 16 diagonal blocks by forward substitution, then T_10
+        if (warp < 2 && lane < 16) {
+            const int j = 16 * warp + lane;
+            float x[16];
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) {
+                float acc = 0.f;
+#pragma unroll
+                for (int ss = 0; ss < ii; ++ss)
+                    if (ss >= lane) acc = fmaf(Af[(16 * warp + ii) * CH + 16 * warp + ss], x[ss], acc);
+                x[ii] = ii < lane ? 0.f : (ii == lane ? 1.f : -acc);
+            }
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) Tf[(16 * warp + ii) * CH + j] = x[ii];
+        }
+        __syncthreads();
+        for (int e = tid; e < 256; e += PT) {  // R = A_10 T_00
+            const int r = e >> 4, cc = e & 15;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc = fmaf(Af[(16 + r) * CH + m], Tf[m * CH + cc], acc);
+            ps.Rt[r][cc] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < 256; e += PT) {  // T_10 = -T_11 R
+            const int r = e >> 4, cc = e & 15;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc = fmaf(Tf[(16 + r) * CH + 16 + m], ps.Rt[m][cc], acc);
+            Tf[(16 + r) * CH + cc] = -acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < CH * CH; e += PT) put_h(r4, tc::op_offset(e / CH, e % CH, CH), Tf[e]);
+
+        // P5: operands from the split k, q rows: (beta e^G k)^T, split e^G q, split (k e^{G_last - G})^T
+        const float Glast = ps.G[CH - 1];
+        for (int t = 0; t < CH; ++t) {
+            const uint32_t ok_ = tc::op_offset(t, tid, PD), oq = tc::op_offset(CH + t, tid, PD);
+            const float kf = get_h(r1, ok_) + get_h(r1 + NR * PD * 2, ok_);
+            const float qf = get_h(r1, oq) + get_h(r1 + NR * PD * 2, oq);
+            put_h(r2 + OP_KBG, tc::op_offset(tid, t, CH), ps.beta[t] * ps.eG[t] * ps.rk[t] * kf);
+            put_split(r3 + OP_QG, r3 + OP_QG + CH * PD * 2, tc::op_offset(t, tid, PD), ps.eG[t] * ps.rq[t] * qf);
+            put_split(r3 + OP_KT, r3 + OP_KT + PD * CH * 2, tc::op_offset(tid, t, CH),
+                      expf(Glast - ps.G[t]) * ps.rk[t] * kf);
+        }
+        publish_smem();
+
+        // P6: W^T = (beta e^G k)^T T^T,  U^T = (beta v)^T T^T  (beta v split)
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t id = tc::idesc_f16(128, CH, false);
+            const uint32_t tb = tc::smem_u32(r4);
+            mma_chain(tm + TM_WT, tc::smem_u32(r2 + OP_KBG), tb, CH, id, false);
+            mma_chain(tm + TM_UT, tc::smem_u32(r2 + OP_VB), tb, CH, id, false);
+            mma_chain(tm + TM_UT, tc::smem_u32(r2 + OP_VB + PD * CH * 2), tb, CH, id, true);
+            tc::mma_commit(&ps.mma_bar);
+        }
+        mma_wait();
+
+        // P7: split M = rq_t rk_s (q.k) e^{G_t - G_s} (s <= t); W operand [t][i] from W^T
+        for (int e = tid; e < CH * CH; e += PT) {
+            const int t = e / CH, s = e % CH;
+            const float m = (s <= t && t < n) ? ps.rq[t] * ps.rk[s] * Gf[(CH + t) * NR + s] * expf(ps.G[t] - ps.G[s]) : 0.f;
+            put_split(r2 + OP_M, r2 + OP_M + CH * CH * 2, tc::op_offset(t, s, CH), m);
+        }
+        for (int t0 = 0; t0 < CH; t0 += 16) {
+            float w[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_WT + t0), w);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) put_h(r1, tc::op_offset(t0 + i, tid, PD), w[i]);
+        }
+        publish_smem();
+
+        // P8: V_new^T = U^T - S^T W^T  (S split)
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t id = tc::idesc_f16(128, CH, true);
+            const uint32_t bw = tc::smem_u32(r1);
+            mma_chain(tm + TM_UT, tc::smem_u32(st_hi), bw, PD, id, true);
+            mma_chain(tm + TM_UT, tc::smem_u32(st_lo), bw, PD, id, true);
+            tc::mma_commit(&ps.mma_bar);
+        }
+        mma_wait();
+
+        // P9: split V_new^T operand; S^T <- e^{G_last} S^T in TMEM
+        for (int t0 = 0; t0 < CH; t0 += 16) {
+            float v[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_UT + t0), v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                put_split(r2 + OP_VN, r2 + OP_VN + PD * CH * 2, tc::op_offset(tid, t0 + i, CH), v[i]);
+        }
+        {
+            const float gam = expf(Glast);
+            for (int i0 = 0; i0 < PD; i0 += 16) {
+                float s[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), s);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) s[i] *= gam;
+                tc::tmem_st16(tc::taddr(tm, lb, TM_ST + i0), s);
+            }
+        }
+        publish_smem();
+
+        // P10: O^T = S^T (e^G q)^T + V_new^T M^T;  S^T += V_new^T (k e^{G_last - G})
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t id32 = tc::idesc_f16(128, CH, false), id128 = tc::idesc_f16(128, PD, false);
+            const uint32_t vh = tc::smem_u32(r2 + OP_VN), vl = tc::smem_u32(r2 + OP_VN + PD * CH * 2);
+            mma_split(tm + TM_OT, tc::smem_u32(st_hi), tc::smem_u32(st_lo), tc::smem_u32(r3 + OP_QG),
+                      tc::smem_u32(r3 + OP_QG + CH * PD * 2), PD, id32, false);
+            mma_split(tm + TM_OT, vh, vl, tc::smem_u32(r2 + OP_M), tc::smem_u32(r2 + OP_M + CH * CH * 2),
+                      CH, id32, true);
+            mma_split(tm + TM_ST, vh, vl, tc::smem_u32(r3 + OP_KT), tc::smem_u32(r3 + OP_KT + PD * CH * 2),
+                      CH, id128, true);
+            tc::mma_commit(&ps.mma_bar);
+        }
+        mma_wait();
+
+        // P11: gated RMSNorm over the head dimension (lane j = channel j) per token
+        float o[CH];
+#pragma unroll
+        for (int t0 = 0; t0 < CH; t0 += 16) {
+            float v[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_OT + t0), v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[t0 + i] = v[i];
+        }
+        float *sq = reinterpret_cast<float *>(r1);
+#pragma unroll
+        for (int t = 0; t < CH; ++t) sq[tid * CH + t] = o[t] * o[t];
+        __syncthreads();
+        {
+            const int t = tid & (CH - 1), quarter = tid >> 5;
+            float s = 0.f;
+            for (int j = 0; j < 32; ++j) s += sq[(quarter * 32 + j) * CH + t];
+            ps.part[quarter][t] = s;
+        }
+        __syncthreads();
+        if (tid < CH)
+            ps.rinv[tid] = 1.0f / sqrtf((ps.part[0][tid] + ps.part[1][tid] + ps.part[2][tid] + ps.part[3][tid]) / PD +
+                                        a.eps_norm);
+        if (ok) ok = mbar_wait_bounded(&ps.z_full, z_ph);
+        z_ph ^= 1u;
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < CH; ++t) {
+            if (t < n) {
+                const float zz = get_bf16(zs, t * PD * 2 + tid * 2);
+                const float y = o[t] * ps.rinv[t] * nw * silu_f(zz);
+                const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + tid;
+                if (a.out_bf16)
+                    reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
+                else
+                    reinterpret_cast<float *>(a.out)[idx] = y;
+            }
+        }
+        __syncthreads();  // the z stage is consumed
+        if (warp == 0 && c0 + CH < T) issue_z(c0 + CH);
+
+        // P12: S^T -> split operand for the next chunk
+        for (int i0 = 0; i0 < PD; i0 += 16) {
+            float s[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), s);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) put_split(st_hi, st_lo, tc::op_offset(tid, i0 + i, PD), s[i]);
+        }
+        publish_smem();
+    }
+
+    // final state S[i][j] from S^T (lane j), and the conv window
+    {
+        float *So = a.state_out + head * PD * PD;
+        for (int i0 = 0; i0 < PD; i0 += 16) {
+            float s[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), s);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) So[(i0 + i) * PD + tid] = s[i];
+        }
+    }
+    if (clustered) cluster_wait_acquire();  // every CTA of the group has read the q/k rows
+#pragma unroll
+    for (int r = 0; r < KM1; ++r) {
+        float *row = a.conv_out + (static_cast<size_t>(b) * KM1 + r) * C;
+        if (qk_owner) {
+            row[chq + tid] = wq[r];
+            row[chk + tid] = wk[r];
+        }
+        row[chv + tid] = wv[r];
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, 512);
+    if (!ok && lane == 0) atomicOr(&g_prefill_error, 1u);
+}
+
+bool chunked_eligible(const gdn_shape_t &s, const StepArgs &a)
+{
+    const int group = s.H_v / s.H_qk;
+    return s.gate_mode == GDN_GATE_PER_HEAD && s.d_k == PD && s.d_v == PD &&
+           s.in_dtype == GDN_BF16 && (s.chunk == CH || s.chunk == 64) && group <= 8 &&
+           (reinterpret_cast<uintptr_t>(a.qkv) & 15u) == 0 &&
+           (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0 && (static_cast<size_t>(a.C) * 2) % 16 == 0;
+}
+
+cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
+{
+    static bool attr_set[64];  // per device; benign race: every writer sets the same value
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(chunk_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.H_v, a.B, 1);
+    cfg.blockDim = dim3(PT, 1, 1);
+    cfg.dynamicSmemBytes = SM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int n = 0;
+    if (a.group > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = a.group;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, chunk_prefill_kernel, a);
+}
+
+}  // namespace
 
 size_t prefill_workspace_bytes(const gdn_shape_t &) { return 0; }
 
 const char *prefill_variant(const gdn_shape_t &s, int num_sms)
 {
+    if (s.gate_mode == GDN_GATE_PER_HEAD && s.d_k == PD && s.d_v == PD && s.in_dtype == GDN_BF16 &&
+        (s.chunk == CH || s.chunk == 64) && s.H_v / s.H_qk <= 8)
+        return "chunked<128,32>";
     StepPlan plan;
     if (!plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms > 0 ? num_sms : 148, &plan))
         return nullptr;
@@ -18,10 +575,22 @@ const char *prefill_variant(const gdn_shape_t &s, int num_sms)
 gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *, int num_sms,
                          cudaStream_t stream)
 {
+    if (chunked_eligible(s, a)) {
+        cudaError_t e = launch_chunked(a, stream);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
     StepPlan plan;
     if (!plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan)) return GDN_ERR_UNSUPPORTED;
     cudaError_t e = launch_step(plan, a, (s.flags & GDN_FLAG_PDL) != 0, num_sms, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+unsigned int take_prefill_error()
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(v)) != cudaSuccess) return ~0u;
+    if (v && cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+    return v;
 }
 
 }  // namespace gdn

@@ -19,4 +19,7 @@ const char *prefill_variant(const gdn_shape_t &s, int num_sms);
 gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspace, int num_sms,
                          cudaStream_t stream);
 
+// Reads and clears the chunked prefill kernel's device error word (synchronous).
+unsigned int take_prefill_error();
+
 }  // namespace gdn

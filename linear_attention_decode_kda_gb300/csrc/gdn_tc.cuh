@@ -4,7 +4,7 @@
 //   * cta_group::1, M = 128: row r of the accumulator D lives in TMEM lane r,
 //     fp32 column c in TMEM column (d_col + c).  Warp w of the CTA reaches the
 //     32 lanes 32 * (w % 4) .. 32 * (w % 4) + 31 with tcgen05.ld / st.
-//   * Operands A (M x K) and B (N x K) are bf16, K-major, in the canonical
+//   * Operands A (M x K) and B (N x K) are 16-bit (fp16 or bf16), K-major, in the canonical
 //     no-swizzle layout of 8 x 8 "core matrices" (8 rows x 16 bytes, stored as
 //     128 contiguous bytes).  Core matrix (row group g, K group q) of an
 //     operand with `kdim` columns sits at byte ((g * (kdim / 8)) + q) * 128, so
@@ -18,7 +18,7 @@
 namespace gdn {
 namespace tc {
 
-// Byte offset of element (r, k) of a K-major canonical operand with kdim columns.
+// Byte offset of 16-bit element (r, k) of a K-major canonical operand with kdim columns.
 __host__ __device__ __forceinline__ uint32_t op_offset(int r, int k, int kdim)
 {
     return static_cast<uint32_t>((((r >> 3) * (kdim >> 3)) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
@@ -38,13 +38,12 @@ __device__ __forceinline__ uint64_t op_desc(uint32_t base, int k0, int kdim)
     return d;                                               // base offset 0, no swizzle
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both K-major.
-__host__ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool negate_a)
+// Instruction descriptor of kind::f16: fp16 (or bf16) A and B, fp32 D, both K-major.
+__host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, bool negate_a, bool bf16 = false)
 {
     uint32_t d = 0;
     d |= 1u << 4;                                    // D format: fp32
-    d |= 1u << 7;                                    // A format: bf16
-    d |= 1u << 10;                                   // B format: bf16
+    if (bf16) d |= (1u << 7) | (1u << 10);           // A, B format: bf16 (0 = fp16)
     if (negate_a) d |= 1u << 13;                     // negate A
     d |= static_cast<uint32_t>(N >> 3) << 17;        // N / 8
     d |= static_cast<uint32_t>(M >> 4) << 24;        // M / 16
@@ -72,7 +71,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 }
 
 // D[tmem] (+)= A * B^T over one K step of 16; issued by a single thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, bool accumulate)
 {
     asm volatile(

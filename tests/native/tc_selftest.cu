@@ -1,5 +1,5 @@
 // Self-test of the tcgen05 helpers in gdn_tc.cuh (test code, not part of the
-// library): one CTA stages A [128 x K] and B [N x K] (bf16, row-major in global
+// library): one CTA stages A [128 x K] and B [N x K] (16-bit, row-major in global
 // memory) into the canonical K-major layout, runs K/16 tcgen05.mma steps into
 // TMEM and reads D back with tcgen05.ld.  mode bit 0: negate A; bit 1: run the
 // K loop twice (D = 2 A B^T); bit 2: preload D0 into TMEM with tcgen05.st and
@@ -52,12 +52,12 @@ tc_selftest_kernel(const __nv_bfloat16 *A, const __nv_bfloat16 *B, const float *
         tc::fence_after_sync();
     }
     if (tid == 0) {
-        const uint32_t idesc = tc::idesc_bf16(128, N, (mode & 1) != 0);
+        const uint32_t idesc = tc::idesc_f16(128, N, (mode & 1) != 0, (mode & 8) == 0);
         const uint32_t a_addr = tc::smem_u32(a_op), b_addr = tc::smem_u32(b_op);
         const int passes = (mode & 2) ? 2 : 1;
         for (int p = 0; p < passes; ++p)
             for (int k0 = 0; k0 < K; k0 += 16)
-                tc::mma_bf16(tbase, tc::op_desc(a_addr, k0, K), tc::op_desc(b_addr, k0, K), idesc,
+                tc::mma_f16(tbase, tc::op_desc(a_addr, k0, K), tc::op_desc(b_addr, k0, K), idesc,
                              (mode & 4) || p > 0 || k0 > 0);
         tc::mma_commit(&bar);
     }

@@ -178,16 +178,22 @@ def test_empty_batch_is_a_no_op():
 
 # ---------------------------------------------------------------- prefill
 
-def _prefill(shape, seed=0, slow=False, tol=PREFILL_TOL):
+def _prefill(shape, seed=0, slow=False, tol=PREFILL_TOL, bf16_out=False, variant=None):
     params, inp, state = _case(shape, shape.T, seed=seed, slow=slow)
-    case = dev.upload(shape, params, inp, state)
-    sh = case.abi_shape()
+    case = dev.upload(shape, params, inp, state, bf16_out=bf16_out)
+    sh = case.abi_shape(bf16_out=bf16_out)
+    if variant is not None:
+        assert gdn.gdn_kernel_variant(sh, gdn.OP_PREFILL) == variant
     nbytes = gdn.gdn_prefill_workspace_bytes(sh)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
     gdn.gdn_prefill_chunked(sh, case.abi_tensors(), ws.data_ptr(), nbytes, stream())
     torch.cuda.synchronize()
+    gdn.gdn_device_status()
     ref = oracle_run(shape, params, inp, state)
-    assert_close(case.out.reshape(ref["y"].shape), ref["y"], tol, "y")
+    if bf16_out:
+        assert_close_bf16_out(case.out.reshape(ref["y"].shape), ref["y"], "y")
+    else:
+        assert_close(case.out.reshape(ref["y"].shape), ref["y"], tol, "y")
     assert_close(case.state, ref["state"], tol, "state")
     assert_close(case.conv_state, ref["conv_state"], 0.0, "conv_state")
 
@@ -195,7 +201,20 @@ def _prefill(shape, seed=0, slow=False, tol=PREFILL_TOL):
 @pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200])
 def test_prefill_ragged_lengths(T):
     shape = synth.Shape(B=2, T=T, H_qk=4, H_v=8, d_k=128, d_v=128, kda=False, chunk=64)
-    _prefill(shape, slow=True)
+    _prefill(shape, slow=True, variant="chunked<128,32>")
+
+
+@pytest.mark.parametrize("H_qk,H_v", [(4, 4), (2, 8)])
+def test_prefill_chunked_head_groups(H_qk, H_v):
+    """Ungrouped heads and four value heads per qk head (thread-block cluster of 4)."""
+    shape = synth.Shape(B=3, T=130, H_qk=H_qk, H_v=H_v, d_k=128, d_v=128, kda=False, chunk=64)
+    _prefill(shape, seed=5, variant="chunked<128,32>")
+    _prefill(shape, seed=6, slow=True)
+
+
+def test_prefill_chunked_bf16_out():
+    shape = synth.Shape(B=2, T=96, H_qk=2, H_v=4, d_k=128, d_v=128, kda=False, chunk=64)
+    _prefill(shape, seed=7, bf16_out=True)
 
 
 def test_prefill_kda_slow_decay():

@@ -1,6 +1,6 @@
 """The tcgen05 building blocks (TMEM alloc, K-major no-swizzle descriptors,
-kind::f16 MMA, commit, tcgen05.ld / st) against a numpy matmul, before the
-chunked prefill relies on them."""
+kind::f16 MMA on bf16 and fp16 inputs, commit, tcgen05.ld / st) against a
+numpy matmul, before the chunked prefill relies on them."""
 
 import ctypes
 import os
@@ -29,11 +29,12 @@ def lib(tmp_path_factory):
 
 
 @pytest.mark.parametrize("K,N", [(16, 64), (64, 64), (128, 64), (128, 128), (64, 128)])
-@pytest.mark.parametrize("mode", [0, 1, 2, 4, 5])
+@pytest.mark.parametrize("mode", [0, 1, 2, 4, 5, 8, 13])
 def test_tcgen05_mma(lib, K, N, mode):
     g = torch.Generator().manual_seed(K * 1000 + N * 10 + mode)
-    A = torch.randn(128, K, generator=g).to(torch.bfloat16)
-    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    dt = torch.float16 if mode & 8 else torch.bfloat16
+    A = torch.randn(128, K, generator=g).to(dt)
+    B = torch.randn(N, K, generator=g).to(dt)
     D0 = torch.randn(128, N, generator=g)
     dA, dB, dD0 = A.cuda(), B.cuda(), D0.cuda()
     dD = torch.full((128, N), float("nan"), device="cuda")
