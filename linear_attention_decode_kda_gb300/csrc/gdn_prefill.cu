@@ -17,14 +17,16 @@
 // as an accumulator, V_new^T, O^T, W^T, U^T too.  The q/k L2 norms come from
 // the diagonal of one Gram product [k; q] [k; q]^T whose off-diagonal blocks
 // give k.k and q.k.  The triangular inverse is a blocked forward substitution
-// in fp32 on the CUDA cores.  One CTA (4 warps) owns one (sequence, value
+// in fp32 on the CUDA cores.  One CTA (8 warps) owns one (sequence, value
 // head); value heads sharing a qk head form a thread-block cluster so the
 // shared q/k conv rows are written only after every CTA has read them.
 #include "gdn_device.cuh"
 #include "gdn_prefill.h"
 #include "gdn_tc.cuh"
 
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 namespace gdn {
 namespace {
@@ -33,12 +35,12 @@ using namespace dev;
 
 constexpr int PD = 128;   // d_k = d_v
 constexpr int CH = 32;    // chunk length
-constexpr int PT = 128;   // threads (4 warps = the 128 TMEM lanes)
+constexpr int PT = 256;   // threads: warps w and w + 4 share TMEM lane quadrant w and split columns
 constexpr int KM1 = 3;
 
 // Dynamic shared memory (bytes).  Regions are reused once their readers are done.
 // Operands marked "split" are stored as fp16 hi and lo halves (x ~ hi + lo).
-constexpr int SM_RAW = 0;                          // [CH][3][PD] bf16 q|k|v rows of the chunk
+constexpr int SM_RAW = 0;                          // [3][CH][PD] bf16 q, k, v rows of the chunk
 constexpr int SM_Z = SM_RAW + CH * 3 * PD * 2;     // [CH][PD] bf16 output-gate rows
 constexpr int SM_ST = SM_Z + CH * PD * 2;          // split S^T [PD x PD]: hi, then lo
 constexpr int SM_R1 = SM_ST + 2 * PD * PD * 2;     // [k; q] hi over [k; q] lo as one 128-row
@@ -47,12 +49,14 @@ constexpr int SM_R2 = SM_R1 + 2 * 2 * CH * PD * 2; // split (beta v)^T, k_bg^T -
 constexpr int SM_R3 = SM_R2 + 3 * PD * CH * 2;     // split (e^G q), split k_t^T
 constexpr int SM_R4 = SM_R3 + 4 * CH * PD * 2;     // T [CH x CH]
 constexpr int SM_R5 = SM_R4 + CH * CH * 2;         // Gram f32 [2CH][2CH], A f32, T f32
-constexpr int SM_BYTES = SM_R5 + 4 * CH * CH * 4 + 2 * CH * CH * 4;
+constexpr int GS = 2 * CH + 1;                     // padded row stride of the f32 Gram
+constexpr int SQS = PD + 1;                         // padded row stride of the o^2 scratch
+constexpr int SM_BYTES = SM_R5 + 2 * CH * GS * 4 + 2 * CH * CH * 4;
 // operand offsets inside the regions
 constexpr int OP_VB = 0, OP_KBG = 2 * PD * CH * 2;                  // R2 (first use)
 constexpr int OP_VN = 0, OP_M = 2 * PD * CH * 2;                    // R2 (second use)
 constexpr int OP_QG = 0, OP_KT = 2 * CH * PD * 2;                   // R3
-constexpr int F_GRAM = 0, F_A = 4 * CH * CH * 4, F_T = F_A + CH * CH * 4;  // R5 (bytes)
+constexpr int F_GRAM = 0, F_A = 2 * CH * GS * 4, F_T = F_A + CH * CH * 4;  // R5 (bytes)
 
 // TMEM columns.
 constexpr int TM_GRAM = 0;    // 128 columns: [k; q]_{hi;lo} [k; q]_{hi;lo}^T
@@ -64,7 +68,7 @@ constexpr int TM_ST = 256;    // 128: S^T
 __device__ unsigned int g_prefill_error;  // bit 0: a bounded mbarrier wait gave up
 
 struct PrefillShared {
-    float G[CH], eG[CH], beta[CH], rk[CH], rq[CH], rinv[CH], part[4][CH];
+    float G[CH], eG[CH], beta[CH], rk[CH], rq[CH], rinv[CH];
     float Rt[16][16];
     uint64_t raw_full, z_full, mma_bar;
     uint32_t tmem;
@@ -89,6 +93,34 @@ __device__ __forceinline__ float get_h(const unsigned char *base, uint32_t off)
 __device__ __forceinline__ float get_bf16(const unsigned char *base, uint32_t off)
 {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
+}
+
+// 8 consecutive K values of one row of a K-major operand (offset 16-byte aligned),
+// as one 128-bit store per half of the split (or of the plain fp16 operand).
+__device__ __forceinline__ void put_row8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *v)
+{
+    __half2 h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half a = __float2half_rn(v[2 * i]), b = __float2half_rn(v[2 * i + 1]);
+        h[i] = __halves2half2(a, b);
+        l[i] = __floats2half2_rn(v[2 * i] - __half2float(a), v[2 * i + 1] - __half2float(b));
+    }
+    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<const uint4 *>(h);
+    if (lo) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<const uint4 *>(l);
+}
+
+// SiLU with the hardware exponential and fast division (relative error ~1e-6,
+// far below the tensor-core operand rounding of this path).
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float conv4_silu_fast(const float4 w, const float *win, float x)
+{
+    float acc = w.x * win[0];
+    acc = fmaf(w.y, win[1], acc);
+    acc = fmaf(w.z, win[2], acc);
+    acc = fmaf(w.w, x, acc);
+    return silu_fast(acc);
 }
 
 // Makes this thread's shared-memory writes visible to the tensor core, then syncs the CTA.
@@ -116,21 +148,25 @@ __device__ __forceinline__ void mma_split(uint32_t d, uint32_t ah, uint32_t al, 
     mma_chain(d, al, bh, kdim, idesc, true);
 }
 
-__global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
+__global__ void __launch_bounds__(PT, 1)
+chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
+                     const __grid_constant__ CUtensorMap tm_z)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ __align__(16) PrefillShared ps;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int ch = tid & (PD - 1);  // channel / TMEM lane of this thread
+    const int lb = 32 * quad;       // this warp's TMEM lane quadrant
     const int h = blockIdx.x, b = blockIdx.y, hq = h / a.group;
     const int T = a.T, C = a.C, H = a.H_v;
     const bool clustered = a.group > 1;
     const bool qk_owner = (h % a.group) == 0;
     const size_t head = static_cast<size_t>(b) * H + h;
-    const int lb = 32 * warp;  // this warp's TMEM lane quadrant; thread tid <-> lane tid
     unsigned char *raw = sm + SM_RAW, *zs = sm + SM_Z;
     unsigned char *st_hi = sm + SM_ST, *st_lo = sm + SM_ST + PD * PD * 2;
     unsigned char *r1 = sm + SM_R1, *r2 = sm + SM_R2, *r3 = sm + SM_R3, *r4 = sm + SM_R4;
-    float *Gf = reinterpret_cast<float *>(sm + SM_R5 + F_GRAM);   // [2CH][2CH]
+    float *Gf = reinterpret_cast<float *>(sm + SM_R5 + F_GRAM);   // [2CH][GS]
     float *Af = reinterpret_cast<float *>(sm + SM_R5 + F_A);      // [CH][CH]
     float *Tf = reinterpret_cast<float *>(sm + SM_R5 + F_T);      // [CH][CH]
     const int chq = hq * PD, chk = a.H_qk * PD + hq * PD, chv = 2 * a.H_qk * PD + h * PD;
@@ -150,62 +186,54 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
     pdl_launch_dependents();
     pdl_wait();
 
-    // parameters and the conv window of channel tid (q, k of qk head hq; v of head h)
+    // parameters and conv windows: half 0 convolves q and k of channel ch, half 1 v
     const float A_h = expf(a.A_log[h]);
     const float dt_h = a.dt_bias[h];
-    const float nw = a.norm_w[tid];
-    const float4 cwq = reinterpret_cast<const float4 *>(a.conv_w)[chq + tid];
-    const float4 cwk = reinterpret_cast<const float4 *>(a.conv_w)[chk + tid];
-    const float4 cwv = reinterpret_cast<const float4 *>(a.conv_w)[chv + tid];
-    float wq[KM1], wk[KM1], wv[KM1];
+    const float nw = a.norm_w[ch];
+    const int c_a = half == 0 ? chq + ch : chv + ch;  // q (half 0) or v (half 1)
+    const int c_b = chk + ch;                         // k (half 0 only)
+    const float4 cwa = reinterpret_cast<const float4 *>(a.conv_w)[c_a];
+    const float4 cwb = reinterpret_cast<const float4 *>(a.conv_w)[c_b];
+    float wa[KM1], wb[KM1];
 #pragma unroll
     for (int r = 0; r < KM1; ++r) {
         const float *row = a.conv_in + (static_cast<size_t>(b) * KM1 + r) * C;
-        wq[r] = row[chq + tid];
-        wk[r] = row[chk + tid];
-        wv[r] = row[chv + tid];
+        wa[r] = row[c_a];
+        wb[r] = row[c_b];
     }
     if (clustered) cluster_arrive_relaxed();  // this CTA has read the shared q/k conv rows
 
-    // state: S[i][j] -> TMEM S^T (lane j = tid, column i) and its split operand copy
+    // state: S[i][j] -> TMEM S^T (lane j = ch, column i) and its split operand copy;
+    // half 0 takes rows i < 64, half 1 the rest
     {
         const float *Sg = a.state_in + head * PD * PD;
-        for (int i0 = 0; i0 < PD; i0 += 16) {
+        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
             float v[16];
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) v[ii] = Sg[(i0 + ii) * PD + tid];
+            for (int ii = 0; ii < 16; ++ii) v[ii] = Sg[(i0 + ii) * PD + ch];
             tc::tmem_st16(tc::taddr(tm, lb, TM_ST + i0), v);
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) put_split(st_hi, st_lo, tc::op_offset(tid, i0 + ii, PD), v[ii]);
+            put_row8(st_hi, st_lo, tc::op_offset(ch, i0, PD), v);
+            put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, PD), v + 8);
         }
     }
 
-    auto issue_raw = [&](int c0) {  // warp 0: q, k, v rows of the chunk at c0
-        const int n = min(CH, T - c0);
+    // q, k, v rows of the chunk at c0: three [CH x PD] boxes of the 2-D view [B*T, C]
+    auto issue_raw = [&](int c0) {
         if (lane == 0) {
             fence_proxy_async_smem();
-            mbar_expect_tx(&ps.raw_full, static_cast<uint32_t>(n) * 3 * PD * 2);
-        }
-        __syncwarp();
-        for (int i = lane; i < 3 * n; i += 32) {
-            const int t = i / 3, sg = i % 3;
-            const int ch = sg == 0 ? chq : (sg == 1 ? chk : chv);
-            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(a.qkv) +
-                                       (static_cast<size_t>(b) * T + c0 + t) * C + ch;
-            tma_load_1d(raw + (t * 3 + sg) * PD * 2, src, PD * 2, &ps.raw_full);
+            mbar_expect_tx(&ps.raw_full, 3 * CH * PD * 2);
+            const int row = b * T + c0;
+            tma_load_2d(raw, &tm_qkv, chq, row, &ps.raw_full);
+            tma_load_2d(raw + CH * PD * 2, &tm_qkv, chk, row, &ps.raw_full);
+            tma_load_2d(raw + 2 * CH * PD * 2, &tm_qkv, chv, row, &ps.raw_full);
         }
     };
-    auto issue_z = [&](int c0) {  // warp 0: output-gate rows of the chunk at c0
-        const int n = min(CH, T - c0);
+    // output-gate rows of the chunk at c0: one [CH x 1 x PD] box of the 3-D view [B*T, H, PD]
+    auto issue_z = [&](int c0) {
         if (lane == 0) {
             fence_proxy_async_smem();
-            mbar_expect_tx(&ps.z_full, static_cast<uint32_t>(n) * PD * 2);
-        }
-        __syncwarp();
-        for (int t = lane; t < n; t += 32) {
-            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(a.z) +
-                                       ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD;
-            tma_load_1d(zs + t * PD * 2, src, PD * 2, &ps.z_full);
+            mbar_expect_tx(&ps.z_full, CH * PD * 2);
+            tma_load_3d(zs, &tm_z, 0, h, b * T + c0, &ps.z_full);
         }
     };
     if (warp == 0) {
@@ -227,6 +255,7 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         mma_ph ^= 1u;
         tc::fence_after_sync();
     };
+    const int t_lo = 16 * half;  // this half's 16 tokens / columns in token-wide phases
 
 #pragma unroll 1
     for (int c0 = 0; c0 < T; c0 += CH) {
@@ -258,23 +287,45 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         raw_ph ^= 1u;
         __syncthreads();
 
-        // P1: conv + SiLU along the chunk for channel tid; split [k; q] rows and (beta v)^T
-        for (int t = 0; t < CH; ++t) {
-            float q = 0.f, k = 0.f, v = 0.f;
-            if (t < n) {
-                const float xq = get_bf16(raw, (t * 3 + 0) * PD * 2 + tid * 2);
-                const float xk = get_bf16(raw, (t * 3 + 1) * PD * 2 + tid * 2);
-                const float xv = get_bf16(raw, (t * 3 + 2) * PD * 2 + tid * 2);
-                q = conv4_silu(cwq, wq, xq);
-                k = conv4_silu(cwk, wk, xk);
-                v = conv4_silu(cwv, wv, xv);
-                wq[0] = wq[1]; wq[1] = wq[2]; wq[2] = xq;
-                wk[0] = wk[1]; wk[1] = wk[2]; wk[2] = xk;
-                wv[0] = wv[1]; wv[1] = wv[2]; wv[2] = xv;
+        // P1: conv + SiLU along the chunk; half 0: split [k; q] rows, half 1: split (beta v)^T.
+        // The chunk's raw values of this thread's channels are read first so the
+        // conv chains of different tokens overlap.
+        if (half == 0) {
+            float xq[CH], xk[CH];
+#pragma unroll
+            for (int t = 0; t < CH; ++t) {
+                xq[t] = get_bf16(raw, (0 * CH + t) * PD * 2 + ch * 2);
+                xk[t] = get_bf16(raw, (1 * CH + t) * PD * 2 + ch * 2);
             }
-            put_split(r1, r1 + NR * PD * 2, tc::op_offset(t, tid, PD), k);
-            put_split(r1, r1 + NR * PD * 2, tc::op_offset(CH + t, tid, PD), q);
-            put_split(r2 + OP_VB, r2 + OP_VB + PD * CH * 2, tc::op_offset(tid, t, CH), ps.beta[t] * v);
+#pragma unroll
+            for (int t = 0; t < CH; ++t) {
+                float q = 0.f, k = 0.f;
+                if (t < n) {
+                    q = conv4_silu_fast(cwa, wa, xq[t]);
+                    k = conv4_silu_fast(cwb, wb, xk[t]);
+                    wa[0] = wa[1]; wa[1] = wa[2]; wa[2] = xq[t];
+                    wb[0] = wb[1]; wb[1] = wb[2]; wb[2] = xk[t];
+                }
+                put_split(r1, r1 + NR * PD * 2, tc::op_offset(t, ch, PD), k);
+                put_split(r1, r1 + NR * PD * 2, tc::op_offset(CH + t, ch, PD), q);
+            }
+        } else {
+            float xv[CH];
+#pragma unroll
+            for (int t = 0; t < CH; ++t) xv[t] = get_bf16(raw, (2 * CH + t) * PD * 2 + ch * 2);
+            float bv[CH];
+#pragma unroll
+            for (int t = 0; t < CH; ++t) {
+                float v = 0.f;
+                if (t < n) {
+                    v = conv4_silu_fast(cwa, wa, xv[t]);
+                    wa[0] = wa[1]; wa[1] = wa[2]; wa[2] = xv[t];
+                }
+                bv[t] = ps.beta[t] * v;
+            }
+#pragma unroll
+            for (int t0 = 0; t0 < CH; t0 += 8)
+                put_row8(r2 + OP_VB, r2 + OP_VB + PD * CH * 2, tc::op_offset(ch, t0, CH), bv + t0);
         }
         publish_smem();
         if (warp == 0 && c0 + CH < T) issue_raw(c0 + CH);  // the raw stage is consumed
@@ -288,34 +339,34 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         }
         mma_wait();
 
-        // P3: exact Gram of [k; q]: hi.hi + hi.lo (rows < NR) + lo.hi (rows >= NR, moved through smem)
-        if (warp >= 2) {
-            for (int s0 = 0; s0 < NR; s0 += 16) {
+        // P3: exact Gram of [k; q]: hi.hi + hi.lo (rows < NR) + lo.hi (rows >= NR, via smem)
+        if (quad >= 2) {
+            for (int s0 = 32 * half; s0 < 32 * half + 32; s0 += 16) {
                 float v[16];
                 tc::tmem_ld16(tc::taddr(tm, lb, TM_GRAM + s0), v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) Gf[(tid - NR) * NR + s0 + i] = v[i];
+                for (int i = 0; i < 16; ++i) Gf[(ch - NR) * GS + s0 + i] = v[i];
             }
         }
         __syncthreads();
-        if (warp < 2) {
-            for (int s0 = 0; s0 < NR; s0 += 16) {
+        if (quad < 2) {
+            for (int s0 = 32 * half; s0 < 32 * half + 32; s0 += 16) {
                 float hh[16], hl[16];
                 tc::tmem_ld16(tc::taddr(tm, lb, TM_GRAM + s0), hh);
                 tc::tmem_ld16(tc::taddr(tm, lb, TM_GRAM + NR + s0), hl);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) Gf[tid * NR + s0 + i] += hh[i] + hl[i];
+                for (int i = 0; i < 16; ++i) Gf[ch * GS + s0 + i] += hh[i] + hl[i];
             }
         }
         __syncthreads();
         if (tid < CH) {
-            ps.rk[tid] = tid < n ? 1.0f / sqrtf(Gf[tid * NR + tid] + a.eps_l2) : 0.f;
-            ps.rq[tid] = tid < n ? a.q_scale / sqrtf(Gf[(CH + tid) * NR + CH + tid] + a.eps_l2) : 0.f;
+            ps.rk[tid] = tid < n ? 1.0f / sqrtf(Gf[tid * GS + tid] + a.eps_l2) : 0.f;
+            ps.rq[tid] = tid < n ? a.q_scale / sqrtf(Gf[(CH + tid) * GS + CH + tid] + a.eps_l2) : 0.f;
         }
         __syncthreads();
         for (int e = tid; e < CH * CH; e += PT) {  // A = beta_t rk_t rk_s (k.k) e^{G_t - G_s}, s < t
             const int t = e / CH, s = e % CH;
-            Af[e] = (s < t && t < n) ? ps.beta[t] * ps.rk[t] * ps.rk[s] * Gf[t * NR + s] * expf(ps.G[t] - ps.G[s]) : 0.f;
+            Af[e] = (s < t && t < n) ? ps.beta[t] * ps.rk[t] * ps.rk[s] * Gf[t * GS + s] * expf(ps.G[t] - ps.G[s]) : 0.f;
             Tf[e] = 0.f;
         }
         __syncthreads();
@@ -336,16 +387,16 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
             for (int ii = 0; ii < 16; ++ii) Tf[(16 * warp + ii) * CH + j] = x[ii];
         }
         __syncthreads();
-        for (int e = tid; e < 256; e += PT) {  // R = A_10 T_00
-            const int r = e >> 4, cc = e & 15;
+        {  // R = A_10 T_00, one element per thread
+            const int r = tid >> 4, cc = tid & 15;
             float acc = 0.f;
 #pragma unroll
             for (int m = 0; m < 16; ++m) acc = fmaf(Af[(16 + r) * CH + m], Tf[m * CH + cc], acc);
             ps.Rt[r][cc] = acc;
         }
         __syncthreads();
-        for (int e = tid; e < 256; e += PT) {  // T_10 = -T_11 R
-            const int r = e >> 4, cc = e & 15;
+        {  // T_10 = -T_11 R
+            const int r = tid >> 4, cc = tid & 15;
             float acc = 0.f;
 #pragma unroll
             for (int m = 0; m < 16; ++m) acc = fmaf(Tf[(16 + r) * CH + 16 + m], ps.Rt[m][cc], acc);
@@ -356,14 +407,22 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
 
         // P5: operands from the split k, q rows: (beta e^G k)^T, split e^G q, split (k e^{G_last - G})^T
         const float Glast = ps.G[CH - 1];
-        for (int t = 0; t < CH; ++t) {
-            const uint32_t ok_ = tc::op_offset(t, tid, PD), oq = tc::op_offset(CH + t, tid, PD);
-            const float kf = get_h(r1, ok_) + get_h(r1 + NR * PD * 2, ok_);
-            const float qf = get_h(r1, oq) + get_h(r1 + NR * PD * 2, oq);
-            put_h(r2 + OP_KBG, tc::op_offset(tid, t, CH), ps.beta[t] * ps.eG[t] * ps.rk[t] * kf);
-            put_split(r3 + OP_QG, r3 + OP_QG + CH * PD * 2, tc::op_offset(t, tid, PD), ps.eG[t] * ps.rq[t] * qf);
-            put_split(r3 + OP_KT, r3 + OP_KT + PD * CH * 2, tc::op_offset(tid, t, CH),
-                      expf(Glast - ps.G[t]) * ps.rk[t] * kf);
+        {
+            float kbg[16], kt[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = t_lo + i;
+                const uint32_t ok_ = tc::op_offset(t, ch, PD), oq = tc::op_offset(CH + t, ch, PD);
+                const float kf = get_h(r1, ok_) + get_h(r1 + NR * PD * 2, ok_);
+                const float qf = get_h(r1, oq) + get_h(r1 + NR * PD * 2, oq);
+                kbg[i] = ps.beta[t] * ps.eG[t] * ps.rk[t] * kf;
+                kt[i] = __expf(Glast - ps.G[t]) * ps.rk[t] * kf;
+                put_split(r3 + OP_QG, r3 + OP_QG + CH * PD * 2, tc::op_offset(t, ch, PD), ps.eG[t] * ps.rq[t] * qf);
+            }
+            put_row8(r2 + OP_KBG, nullptr, tc::op_offset(ch, t_lo, CH), kbg);
+            put_row8(r2 + OP_KBG, nullptr, tc::op_offset(ch, t_lo + 8, CH), kbg + 8);
+            put_row8(r3 + OP_KT, r3 + OP_KT + PD * CH * 2, tc::op_offset(ch, t_lo, CH), kt);
+            put_row8(r3 + OP_KT, r3 + OP_KT + PD * CH * 2, tc::op_offset(ch, t_lo + 8, CH), kt + 8);
         }
         publish_smem();
 
@@ -382,14 +441,14 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         // P7: split M = rq_t rk_s (q.k) e^{G_t - G_s} (s <= t); W operand [t][i] from W^T
         for (int e = tid; e < CH * CH; e += PT) {
             const int t = e / CH, s = e % CH;
-            const float m = (s <= t && t < n) ? ps.rq[t] * ps.rk[s] * Gf[(CH + t) * NR + s] * expf(ps.G[t] - ps.G[s]) : 0.f;
+            const float m = (s <= t && t < n) ? ps.rq[t] * ps.rk[s] * Gf[(CH + t) * GS + s] * expf(ps.G[t] - ps.G[s]) : 0.f;
             put_split(r2 + OP_M, r2 + OP_M + CH * CH * 2, tc::op_offset(t, s, CH), m);
         }
-        for (int t0 = 0; t0 < CH; t0 += 16) {
+        {
             float w[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_WT + t0), w);
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_WT + t_lo), w);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) put_h(r1, tc::op_offset(t0 + i, tid, PD), w[i]);
+            for (int i = 0; i < 16; ++i) put_h(r1, tc::op_offset(t_lo + i, ch, PD), w[i]);
         }
         publish_smem();
 
@@ -405,21 +464,20 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         mma_wait();
 
         // P9: split V_new^T operand; S^T <- e^{G_last} S^T in TMEM
-        for (int t0 = 0; t0 < CH; t0 += 16) {
+        {
             float v[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_UT + t0), v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                put_split(r2 + OP_VN, r2 + OP_VN + PD * CH * 2, tc::op_offset(tid, t0 + i, CH), v[i]);
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_UT + t_lo), v);
+            put_row8(r2 + OP_VN, r2 + OP_VN + PD * CH * 2, tc::op_offset(ch, t_lo, CH), v);
+            put_row8(r2 + OP_VN, r2 + OP_VN + PD * CH * 2, tc::op_offset(ch, t_lo + 8, CH), v + 8);
         }
         {
             const float gam = expf(Glast);
-            for (int i0 = 0; i0 < PD; i0 += 16) {
-                float s[16];
-                tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), s);
+            for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+                float sv[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), sv);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) s[i] *= gam;
-                tc::tmem_st16(tc::taddr(tm, lb, TM_ST + i0), s);
+                for (int i = 0; i < 16; ++i) sv[i] *= gam;
+                tc::tmem_st16(tc::taddr(tm, lb, TM_ST + i0), sv);
             }
         }
         publish_smem();
@@ -439,38 +497,34 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         }
         mma_wait();
 
-        // P11: gated RMSNorm over the head dimension (lane j = channel j) per token
-        float o[CH];
+        // P11: gated RMSNorm over the head dimension per token; this thread holds
+        // o of channel ch for tokens t_lo .. t_lo + 15
+        float o[16];
+        tc::tmem_ld16(tc::taddr(tm, lb, TM_OT + t_lo), o);
+        float *sq = reinterpret_cast<float *>(r1);  // [CH][SQS], token-major
 #pragma unroll
-        for (int t0 = 0; t0 < CH; t0 += 16) {
-            float v[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_OT + t0), v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[t0 + i] = v[i];
-        }
-        float *sq = reinterpret_cast<float *>(r1);
-#pragma unroll
-        for (int t = 0; t < CH; ++t) sq[tid * CH + t] = o[t] * o[t];
+        for (int i = 0; i < 16; ++i) sq[(t_lo + i) * SQS + ch] = o[i] * o[i];
         __syncthreads();
         {
-            const int t = tid & (CH - 1), quarter = tid >> 5;
-            float s = 0.f;
-            for (int j = 0; j < 32; ++j) s += sq[(quarter * 32 + j) * CH + t];
-            ps.part[quarter][t] = s;
+            const int t = tid >> 3, part = tid & 7;
+            float s_ = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s_ += sq[t * SQS + 16 * part + j];
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 1);
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 2);
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 4);
+            if (part == 0) ps.rinv[t] = 1.0f / sqrtf(s_ / PD + a.eps_norm);
         }
-        __syncthreads();
-        if (tid < CH)
-            ps.rinv[tid] = 1.0f / sqrtf((ps.part[0][tid] + ps.part[1][tid] + ps.part[2][tid] + ps.part[3][tid]) / PD +
-                                        a.eps_norm);
         if (ok) ok = mbar_wait_bounded(&ps.z_full, z_ph);
         z_ph ^= 1u;
         __syncthreads();
 #pragma unroll
-        for (int t = 0; t < CH; ++t) {
+        for (int i = 0; i < 16; ++i) {
+            const int t = t_lo + i;
             if (t < n) {
-                const float zz = get_bf16(zs, t * PD * 2 + tid * 2);
-                const float y = o[t] * ps.rinv[t] * nw * silu_f(zz);
-                const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + tid;
+                const float zz = get_bf16(zs, t * PD * 2 + ch * 2);
+                const float y = o[i] * ps.rinv[t] * nw * silu_fast(zz);
+                const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + ch;
                 if (a.out_bf16)
                     reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
                 else
@@ -481,11 +535,11 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
         if (warp == 0 && c0 + CH < T) issue_z(c0 + CH);
 
         // P12: S^T -> split operand for the next chunk
-        for (int i0 = 0; i0 < PD; i0 += 16) {
-            float s[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), s);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) put_split(st_hi, st_lo, tc::op_offset(tid, i0 + i, PD), s[i]);
+        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+            float sv[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), sv);
+            put_row8(st_hi, st_lo, tc::op_offset(ch, i0, PD), sv);
+            put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, PD), sv + 8);
         }
         publish_smem();
     }
@@ -493,22 +547,25 @@ __global__ void __launch_bounds__(PT, 1) chunk_prefill_kernel(const StepArgs a)
     // final state S[i][j] from S^T (lane j), and the conv window
     {
         float *So = a.state_out + head * PD * PD;
-        for (int i0 = 0; i0 < PD; i0 += 16) {
-            float s[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), s);
+        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+            float sv[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_ST + i0), sv);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) So[(i0 + i) * PD + tid] = s[i];
+            for (int i = 0; i < 16; ++i) So[(i0 + i) * PD + ch] = sv[i];
         }
     }
     if (clustered) cluster_wait_acquire();  // every CTA of the group has read the q/k rows
 #pragma unroll
     for (int r = 0; r < KM1; ++r) {
         float *row = a.conv_out + (static_cast<size_t>(b) * KM1 + r) * C;
-        if (qk_owner) {
-            row[chq + tid] = wq[r];
-            row[chk + tid] = wk[r];
+        if (half == 0) {
+            if (qk_owner) {
+                row[c_a] = wa[r];
+                row[c_b] = wb[r];
+            }
+        } else {
+            row[c_a] = wa[r];
         }
-        row[chv + tid] = wv[r];
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -522,7 +579,23 @@ bool chunked_eligible(const gdn_shape_t &s, const StepArgs &a)
     return s.gate_mode == GDN_GATE_PER_HEAD && s.d_k == PD && s.d_v == PD &&
            s.in_dtype == GDN_BF16 && (s.chunk == CH || s.chunk == 64) && group <= 8 &&
            (reinterpret_cast<uintptr_t>(a.qkv) & 15u) == 0 &&
-           (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0 && (static_cast<size_t>(a.C) * 2) % 16 == 0;
+           (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0 && (static_cast<size_t>(a.C) * 2) % 16 == 0 &&
+           static_cast<long long>(a.B) * a.T < (1LL << 31);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;  // benign race: same value
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
 }
 
 cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
@@ -537,6 +610,28 @@ cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
                                  SM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap tq, tz;
+    const cuuint64_t rows = static_cast<cuuint64_t>(a.B) * a.T;
+    {   // qkv as [B*T rows][C channels] bf16, boxes of CH rows x PD channels
+        const cuuint64_t dim[2] = {static_cast<cuuint64_t>(a.C), rows};
+        const cuuint64_t stride[1] = {static_cast<cuuint64_t>(a.C) * 2};
+        const cuuint32_t box[2] = {PD, CH}, estride[2] = {1, 1};
+        if (encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.qkv), dim, stride, box,
+                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {   // z as [B*T][H_v][PD] bf16, boxes of CH tokens x 1 head x PD channels
+        const cuuint64_t dim[3] = {PD, static_cast<cuuint64_t>(a.H_v), rows};
+        const cuuint64_t stride[2] = {PD * 2, static_cast<cuuint64_t>(a.H_v) * PD * 2};
+        const cuuint32_t box[3] = {PD, 1, CH}, estride[3] = {1, 1, 1};
+        if (encode(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.z), dim, stride, box,
+                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.H_v, a.B, 1);
@@ -554,7 +649,7 @@ cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, chunk_prefill_kernel, a);
+    return cudaLaunchKernelEx(&cfg, chunk_prefill_kernel, a, tq, tz);
 }
 
 }  // namespace
