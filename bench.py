@@ -28,6 +28,7 @@ import dataclasses
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import time
@@ -283,7 +284,6 @@ class SingleLaunch(Workload):
         self.launches_per_step = 1
         self.units_per_step = s.B * s.T
         self.bytes_per_launch = algorithmic_bytes(s, verify=(op == gdn.OP_VERIFY))
-        self.flops_per_launch = prefill_flops(s) if op == gdn.OP_PREFILL else 0.0
         params = synth.make_params(s)
         state = synth.make_state(s)
         n = n_inputs if op == gdn.OP_DECODE else 1
@@ -306,6 +306,10 @@ class SingleLaunch(Workload):
         self.host_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         self.abi_shape = self.case.abi_shape()
         self.kernel = gdn.gdn_kernel_variant(self.abi_shape, op)
+        # dense products of the chunked form at the chunk length the kernel runs
+        m = re.match(r"chunked<\d+,(\d+)>", self.kernel or "") if op == gdn.OP_PREFILL else None
+        self.flops_per_launch = (prefill_flops(dataclasses.replace(s, chunk=int(m.group(1))))
+                                 if m else 0.0)
         self.ws_bytes = gdn.gdn_prefill_workspace_bytes(self.abi_shape) if op == 2 else 0
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         self.h2d_bytes = sum(v[0].numel() * v.element_size() for v in self.dev_in.values())
@@ -355,6 +359,26 @@ def make_workload(name, device):
     return SingleLaunch(name, spec, device, op)
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(values, world: int, device=None) -> list:
+    """Per-rank elapsed times (ms) -> their maximum over all ranks (every rank
+    gets the same list).  One rank: unchanged.  Uses the default process group."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Units all ranks processed (each rank runs its own full workload: weak
+    scaling) per second of the slowest rank's time."""
+    return units_per_step * steps * world / (ms * 1e-3)
+
+
 # ---------------------------------------------------------------- timing
 
 def time_steps(fn, warmup, steps, flush):
@@ -387,22 +411,39 @@ def roofline(w: Workload, ms_per_step: float, peaks: dict) -> dict:
 
 # ---------------------------------------------------------------- CPU oracle legs
 
-def oracle_decode_rate(name: str, tokens: int, nthreads: int) -> dict:
-    """The fp64 oracle on a bounded sample of the workload: layer-steps/s."""
+def oracle_decode_rate(name: str, tokens: int, nthreads: int, target_s: float = 12.0,
+                       max_passes: int = 64) -> dict:
+    """The fp64 oracle on a bounded sample of the workload: layer-steps/s.
+
+    Every layer of the workload advances `tokens` tokens per pass (one oracle
+    call per layer, threads over the (sequence, head) units); passes repeat,
+    carrying the state, until about `target_s` seconds of oracle time.
+    Generating the inputs is not timed.
+    """
     import oracle
     spec = synth.WORKLOADS[name]
     s = spec["shape"]
     layers = spec["layers"]
     sT = dataclasses.replace(s, T=tokens)
-    cases = [(synth.make_params(s, layer=l), synth.make_inputs(sT, layer=l),
-              synth.make_state(s, layer=l)) for l in range(layers)]
-    t0 = time.perf_counter()
-    for p, i, st in cases:
-        oracle.run(sT, p, i, st.conv, st.S, nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    return {"value": round(layers * s.B * tokens / dt, 2), "unit": UNIT,
+    cases = []
+    for l in range(layers):
+        st = synth.make_state(s, layer=l)
+        cases.append([synth.make_params(s, layer=l), synth.make_inputs(sT, layer=l),
+                      st.conv, st.S])
+    lib = oracle.load()
+    dt, passes = 0.0, 0
+    while passes < max_passes and (passes == 0 or dt < target_s):
+        for c in cases:
+            t0 = time.perf_counter()
+            r = oracle.run(sT, c[0], c[1], c[2], c[3], nthreads=nthreads, lib=lib)
+            dt += time.perf_counter() - t0
+            c[2], c[3] = r["conv_state"], r["state"]
+        passes += 1
+    steps = passes * layers * s.B * tokens
+    return {"value": round(steps / dt, 2), "unit": UNIT,
             "cores": min(nthreads, s.B * s.H_v), "kind": "oracle",
-            "sample": f"{layers} layers x {tokens} tokens of {name} (fp64 C, threads over heads)",
+            "sample": f"{passes} passes x {layers} layers x {tokens} tokens of {name} "
+                      f"(fp64 C, threads over (sequence, head) units; state carried)",
             "seconds": round(dt, 2)}
 
 
@@ -500,14 +541,11 @@ def run_ours(args):
     with ClockSampler(str(uuid) if uuid else None) as clk:
         ms = time_steps(main.step, args.warmup, args.steps, flush)
     ms_e2e = time_steps(main.e2e_step, args.warmup, args.steps, flush)
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, device)
     if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
         dist.barrier()
 
-    units = main.units_per_step * args.steps * world
-    value = units / (ms * 1e-3)
+    value = whole_job_rate(main.units_per_step, args.steps, world, ms)
     ms_step = ms / args.steps
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -524,7 +562,8 @@ def run_ours(args):
                        if isinstance(main, DecodeLayers) else "one ABI call per step",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline(main, ms_step, peaks),
-            "e2e": {"value": round(units / (ms_e2e * 1e-3), 2), "unit": UNIT,
+            "e2e": {"value": round(whole_job_rate(main.units_per_step, args.steps, world,
+                                                  ms_e2e), 2), "unit": UNIT,
                     "h2d_bytes_per_step": main.h2d_bytes, "d2h_bytes_per_step": main.d2h_bytes},
             "gpu_launches": main.launches_per_step * args.steps,
             "clocks": clk.summary()}
@@ -567,7 +606,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--aux-steps", type=int, default=100)
-    ap.add_argument("--cpu-tokens", type=int, default=96)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
