@@ -5,7 +5,7 @@
 // is per head) on tcgen05 tensor cores.  Other shapes run the T tokens
 // through the recurrent step kernel.
 //
-// Per chunk of C = 64 tokens with start state S0 (G_t = cumulative log-decay
+// Per chunk of C = 32 tokens with start state S0 (G_t = cumulative log-decay
 // inside the chunk, every exponent <= 0):
 //   A[t][s] = beta_t (k_t . k_s) e^{G_t - G_s}   (s < t),   T = (I + A)^-1
 //   W = T (beta e^G k),  U = T (beta v),  V_new = U - W S0
@@ -23,10 +23,10 @@
 #include "gdn_device.cuh"
 #include "gdn_prefill.h"
 #include "gdn_tc.cuh"
+#include "gdn_tmap.h"
 
 #include <cuda.h>
 #include <cuda_fp16.h>
-#include <cudaTypedefs.h>
 
 namespace gdn {
 namespace {
@@ -583,21 +583,6 @@ bool chunked_eligible(const gdn_shape_t &s, const StepArgs &a)
            static_cast<long long>(a.B) * a.T < (1LL << 31);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;  // benign race: same value
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
 {
     static bool attr_set[64];  // per device; benign race: every writer sets the same value
@@ -611,26 +596,20 @@ cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
     CUtensorMap tq, tz;
-    const cuuint64_t rows = static_cast<cuuint64_t>(a.B) * a.T;
+    const uint64_t rows = static_cast<uint64_t>(a.B) * a.T;
     {   // qkv as [B*T rows][C channels] bf16, boxes of CH rows x PD channels
-        const cuuint64_t dim[2] = {static_cast<cuuint64_t>(a.C), rows};
-        const cuuint64_t stride[1] = {static_cast<cuuint64_t>(a.C) * 2};
-        const cuuint32_t box[2] = {PD, CH}, estride[2] = {1, 1};
-        if (encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.qkv), dim, stride, box,
-                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        const uint64_t dim[2] = {static_cast<uint64_t>(a.C), rows};
+        const uint64_t stride[1] = {static_cast<uint64_t>(a.C) * 2};
+        const uint32_t box[2] = {PD, CH};
+        if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qkv, dim, stride, box))
             return cudaErrorInvalidValue;
     }
     {   // z as [B*T][H_v][PD] bf16, boxes of CH tokens x 1 head x PD channels
-        const cuuint64_t dim[3] = {PD, static_cast<cuuint64_t>(a.H_v), rows};
-        const cuuint64_t stride[2] = {PD * 2, static_cast<cuuint64_t>(a.H_v) * PD * 2};
-        const cuuint32_t box[3] = {PD, 1, CH}, estride[3] = {1, 1, 1};
-        if (encode(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.z), dim, stride, box,
-                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        const uint64_t dim[3] = {PD, static_cast<uint64_t>(a.H_v), rows};
+        const uint64_t stride[2] = {PD * 2, static_cast<uint64_t>(a.H_v) * PD * 2};
+        const uint32_t box[3] = {PD, 1, CH};
+        if (!encode_tiled(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.z, dim, stride, box))
             return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};
