@@ -141,6 +141,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Waits (acquire at cluster scope) for phase `parity` of a local mbarrier that
+// remote CTAs complete with st.async; gives up after about two seconds.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (i >= 256u) __nanosleep(32);
+    }
+    return false;
+}
+
+// Writes v into the word at `slot`'s offset inside CTA `rank` of the cluster and
+// completes 4 bytes of transactions on the mbarrier at `bar`'s offset there.
+__device__ __forceinline__ void st_async_remote(float *slot, uint32_t rank, float v, uint64_t *bar)
+{
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(slot)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+                 "r"(__float_as_uint(v)), "r"(rb)
+                 : "memory");
+}
+
 // One bulk global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned) that completes `bytes` transactions on `bar`.
 __device__ __forceinline__ void tma_load_1d(void *dst_smem, const void *src_gmem, uint32_t bytes,

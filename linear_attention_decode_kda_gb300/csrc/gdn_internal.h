@@ -42,8 +42,9 @@ bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
 bool stream_eligible(const StepArgs &a);
 cudaError_t launch_stream(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
 
-// Reads and clears the streaming kernel's device error word (synchronous).
+// Read and clear the step kernels' device error words (synchronous).
 unsigned int take_stream_error();
+unsigned int take_step_error();
 
 // The plan for B*H_v units on a GPU with `num_sms` SMs.  Decode and verify of
 // the same (B, H_v) always get the same plan, so their per-token arithmetic

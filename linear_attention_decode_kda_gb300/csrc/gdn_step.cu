@@ -37,6 +37,8 @@ using namespace dev;
 
 constexpr int KM1 = 3;  // conv window rows kept between calls (conv_K - 1)
 
+__device__ unsigned int g_step_error;  // bit 0: a bounded mbarrier wait gave up
+
 template <int CQ, int CV>
 struct TokenIn {
     float xq[CQ], xk[CQ], fq[CQ], xv[CV];
@@ -70,14 +72,22 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     __shared__ __align__(16) float red_k[NWARP][W];
     __shared__ __align__(16) float red_q[NWARP][W];
     __shared__ float rms_slot[2][NSLAB];
+    __shared__ __align__(8) uint64_t rms_bar[2];  // completed by the slabs' pushes of token parity
     __shared__ float beta_s;
 
     pdl_launch_dependents();
     uint32_t rank0 = 0;  // cluster rank of slab 0 of this head
     if (clustered) {
         rank0 = cluster_rank() - slab;
+        if (tid == 0) {
+            mbar_init(&rms_bar[0], 1);
+            mbar_init(&rms_bar[1], 1);
+            fence_mbar_init();
+        }
         cluster_arrive_relaxed();
     }
+
+    bool ok = true;  // false once a bounded wait gave up
 
     // ---- before the dependency wait: state slab, conv windows, parameters
     const size_t head = static_cast<size_t>(b) * a.H_v + h;
@@ -269,35 +279,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             o[c] = fmaf(kq, u[c], qS[c]);
         }
 
-        // 4. gated RMSNorm over the head's D columns
-        float p = 0.f;
-        if (warp == 0) {
-            if (rg == 0) p = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-        }
-        float total = p;
-        if (clustered) {
-            if (t == 0) cluster_wait_acquire();  // every CTA of the cluster has started
-            if (tid == 0) {
-#pragma unroll
-                for (int s = 0; s < NSLAB; ++s) dsmem_store(&rms_slot[t & 1][slab], rank0 + s, p);
-            }
-            cluster_arrive_release();
-            cluster_wait_acquire();
-            total = 0.f;
-#pragma unroll
-            for (int s = 0; s < NSLAB; ++s) total += rms_slot[t & 1][s];
-        }
-        if (rg == 0) {
-            const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
-            float y[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) y[c] = o[c] * rinv * nw[c] * silu_f(cur.z[c]);
-            store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
-        }
-
-        // 5. state update and stores
+        // 4. state update and stores (they do not wait for the RMS exchange)
         const bool last = (t == a.T - 1);
         float *hist = a.state_hist
             ? a.state_hist + ((static_cast<size_t>(t) * a.B + b) * a.H_v + h) * D * D + col0
@@ -314,6 +296,39 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             const size_t off = static_cast<size_t>(row) * D;
             if (hist) __stcs(reinterpret_cast<float4 *>(hist + off), st[r]);
             if (commit) __stcs(reinterpret_cast<float4 *>(commit + off), st[r]);
+        }
+
+        // 5. gated RMSNorm over the head's D columns.  The D / W slabs push their
+        //    partial sums of o^2 into every slab's slot for this token parity and
+        //    complete 4 bytes each on that slab's mbarrier; a slab can be at most one
+        //    token ahead of the slowest (it needs every partial to finish a token).
+        float p = 0.f;
+        if (warp == 0) {
+            if (rg == 0) p = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        }
+        float total = p;
+        if (clustered) {
+            if (t == 0) cluster_wait_acquire();  // every CTA of the cluster has set up its barriers
+            if (tid == 0) {
+                mbar_expect_tx(&rms_bar[t & 1], NSLAB * 4);
+#pragma unroll
+                for (int s = 0; s < NSLAB; ++s) st_async_remote(&rms_slot[t & 1][slab], rank0 + s, p, &rms_bar[t & 1]);
+            }
+            if (rg == 0) {
+                ok &= mbar_wait_cluster_bounded(&rms_bar[t & 1], static_cast<uint32_t>(t >> 1) & 1u);
+                total = 0.f;
+#pragma unroll
+                for (int s = 0; s < NSLAB; ++s) total += rms_slot[t & 1][s];
+            }
+        }
+        if (rg == 0) {
+            const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
+            float y[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) y[c] = o[c] * rinv * nw[c] * silu_f(cur.z[c]);
+            store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
         }
 
         // conv window after this token (verify history)
@@ -344,8 +359,19 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         cur = nxt;
     }
 
-    // final conv window (commit); every reader of the shared q/k rows has
-    // passed the last cluster barrier (or is this CTA)
+    // final conv window (commit), after every reader of the shared q/k rows:
+    // grouped heads pass a cluster barrier; the slabs of one head have each
+    // pushed partial sums computed from their window reads, all of which this
+    // CTA's waiting threads have received
+    if (clustered) {
+        if (a.group > 1) {
+            cluster_arrive_release();
+            cluster_wait_acquire();
+        } else {
+            __syncthreads();
+        }
+    }
+    if (!ok) atomicOr(&g_step_error, 1u);
     if (a.conv_out) {
         float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
 #pragma unroll
@@ -447,6 +473,14 @@ cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaS
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, v->fn, a);
+}
+
+unsigned int take_step_error()
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_step_error, sizeof(v)) != cudaSuccess) return ~0u;
+    if (v && cudaMemcpyToSymbol(g_step_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+    return v;
 }
 
 }  // namespace gdn
