@@ -195,6 +195,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, in
         : "memory");
 }
 
+// Brings a tensor map (a __grid_constant__ kernel parameter) into the TMA descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, int x, int y, int z,
                                             uint64_t *bar)
 {

@@ -8,11 +8,11 @@
 // memory ahead of its turn, completing on mbarriers:
 //   * the 64 KiB fp32 state tile (one bulk copy): one stage per CTA, refilled
 //     with the CTA's next head as soon as the current tile is in registers;
-//   * the head's inputs and parameters in eight copies -- q/k/v rows, conv
-//     window, conv weights, gate rows, output-gate rows and beta through
-//     tensor maps (each copy spans all T tokens or all three q/k/v segments),
-//     dt_bias and A_log as bulk copies -- into a ring of input stages, each
-//     refilled as soon as its head's last token has read it.
+//   * the head's inputs and parameters in ten copies -- q/k/v rows, conv
+//     window, gate rows, output-gate rows and beta through tensor maps (each
+//     copy spans all T tokens or all three q/k/v segments), the three 2 KiB
+//     runs of conv weights, dt_bias and A_log as bulk copies -- into a ring of
+//     input stages, each refilled as soon as its head's last token has read it.
 // With the memory system saturated a single load waits several microseconds,
 // so nothing on a head's critical path is fetched on demand; and with two
 // CTAs per SM one CTA's stores overlap the other's arithmetic.
@@ -82,7 +82,6 @@ __host__ __device__ __forceinline__ uint32_t input_bytes(int T, int es, int kda)
 struct InMaps {
     CUtensorMap qkv;   // {SD*H, 3, B*T}: box {SD, 3, T} -> q, k, v rows of T tokens
     CUtensorMap win;   // {SD*H, 3, B*3}: box {SD, 3, 3} -> the head's conv window
-    CUtensorMap cw;    // {4, SD*H, 3}:   box {4, SD, 3} -> conv weights of q, k, v
     CUtensorMap f;     // per channel {SD, H, B*T} box {SD, 1, T}; per head {H, B*T} box {16/es, T}
     CUtensorMap z;     // {SD, H, B*T}:   box {SD, 1, T}
     CUtensorMap beta;  // {H, B*T}:       box {16/es, T}
@@ -123,7 +122,12 @@ __device__ __forceinline__ void issue_inputs(const StepArgs &a, const InMaps &m,
     switch (lane) {
     case 0: tma_load_3d(stage + L.qkv, &m.qkv, h * SD, 0, bt, bar); break;
     case 1: tma_load_3d(stage + L.win, &m.win, h * SD, 0, b * KM1, bar); break;
-    case 2: tma_load_3d(stage + L.cw, &m.cw, 0, h * SD, 0, bar); break;
+    case 2:  // conv weights of the head's q, k and v channels: 2 KiB contiguous each
+        for (int sg = 0; sg < 3; ++sg)
+            tma_load_1d(stage + L.cw + sg * SD * 16,
+                        a.conv_w + (static_cast<size_t>(sg) * a.H_qk * SD + static_cast<size_t>(h) * SD) * 4,
+                        SD * 16, bar);
+        break;
     case 3:
         if (a.kda) tma_load_3d(stage + L.f, &m.f, 0, h, bt, bar);
         else tma_load_2d(stage + L.f, &m.f, h & ~(per16 - 1), bt, bar);
@@ -178,6 +182,13 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
         tma_load_1d(tile, a.state_in + static_cast<size_t>(c0) * SD * SD, TILE_BYTES, &sh.tile_full);
     }
     const float nw = qk_thr ? 0.0f : a.norm_w[ch];
+    if (tid == 0) {  // the input maps' descriptors, ahead of their first use
+        prefetch_tensormap(&maps.qkv);
+        prefetch_tensormap(&maps.win);
+        prefetch_tensormap(&maps.f);
+        prefetch_tensormap(&maps.z);
+        prefetch_tensormap(&maps.beta);
+    }
     pdl_wait();  // inputs may be written by the previous kernel on the stream
     if (warp == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -462,12 +473,6 @@ cudaError_t launch_stream(const StepPlan &plan, const StepArgs &a, bool pdl, cud
         const uint64_t str[2] = {H * SD * 4, static_cast<uint64_t>(a.C) * 4};
         const uint32_t box[3] = {SD, 3, KM1};
         ok = ok && encode_tiled(&m.win, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.conv_in, dim, str, box);
-    }
-    {   // conv weights: {tap, channel within segment, segment}
-        const uint64_t dim[3] = {4, H * SD, 3};
-        const uint64_t str[2] = {16, H * SD * 16};
-        const uint32_t box[3] = {4, SD, 3};
-        ok = ok && encode_tiled(&m.cw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.conv_w, dim, str, box);
     }
     {   // rows of SD per (token, head): z, and the gate rows when per channel
         const uint64_t dim[3] = {SD, H, BT};
