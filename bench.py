@@ -48,21 +48,24 @@ FLUSH_BYTES = 512 << 20
 
 # ---------------------------------------------------------------- bytes and peaks
 
-def algorithmic_bytes(s: synth.Shape, verify: bool = False) -> int:
+def algorithmic_bytes(s: synth.Shape, mode: str = "decode") -> int:
     """Bytes one call must move at minimum in this ABI's layouts.
 
-    state read + write (verify: read once, write T per-token states), conv
-    window read + write (K-1 rows each, shifted layout), conv weights, the
-    inputs, the parameters and the output (fp32).
+    decode / prefill: state read + write, conv window read + write (K-1 rows
+    each, shifted layout); verify: state read once, T per-token states
+    written, window read; verify_outputs: state and window read only; commit
+    (out not written): state and window read + write.  Plus conv weights, the
+    inputs, the parameters and the fp32 output where it is written.
     """
     ib = 2 if s.bf16_in else 4
     state = s.B * s.H_v * s.d_k * s.d_v * 4
     conv = s.B * (s.K - 1) * s.C * 4
-    st_bytes = state * (1 + s.T) if verify else 2 * state
-    conv_bytes = conv if verify else 2 * conv
+    st_bytes = {"decode": 2 * state, "prefill": 2 * state, "verify": state * (1 + s.T),
+                "verify_outputs": state, "commit": 2 * state}[mode]
+    conv_bytes = conv if mode in ("verify", "verify_outputs") else 2 * conv
     inputs = s.B * s.T * (s.C + s.H_v * s.f_width + s.H_v + s.H_v * s.d_v) * ib
     params = s.C * s.K * 4 + s.H_v * 4 + s.H_v * (s.d_k if s.kda else 1) * 4 + s.d_v * 4
-    out = s.B * s.T * s.H_v * s.d_v * 4
+    out = 0 if mode == "commit" else s.B * s.T * s.H_v * s.d_v * 4
     return st_bytes + conv_bytes + inputs + params + out
 
 
@@ -274,16 +277,18 @@ class DecodeLayers(Workload):
 class SingleLaunch(Workload):
     """Batched decode, verify or prefill: one ABI call per step."""
 
-    def __init__(self, name, spec, device, op, n_inputs=8):
+    def __init__(self, name, spec, device, mode, n_inputs=8):
         import torch
 
         import linear_attention_decode_kda_gb300 as gdn
         from synth import device as dev
         s = spec["shape"]
-        self.name, self.shape, self.op, self.gdn = name, s, op, gdn
+        op = {"decode": gdn.OP_DECODE, "verify": gdn.OP_VERIFY, "verify_outputs": gdn.OP_VERIFY,
+              "commit": gdn.OP_VERIFY, "prefill": gdn.OP_PREFILL}[mode]
+        self.name, self.shape, self.op, self.mode, self.gdn = name, s, op, mode, gdn
         self.launches_per_step = 1
         self.units_per_step = s.B * s.T
-        self.bytes_per_launch = algorithmic_bytes(s, verify=(op == gdn.OP_VERIFY))
+        self.bytes_per_launch = algorithmic_bytes(s, mode)
         params = synth.make_params(s)
         state = synth.make_state(s)
         n = n_inputs if op == gdn.OP_DECODE else 1
@@ -300,8 +305,7 @@ class SingleLaunch(Workload):
         self.dev_in = {k: dev.to_torch(v, bf, device) for k, v in host.items()}
         self.host_in = {k: dev.to_torch(v, bf, None).pin_memory() for k, v in host.items()}
         first = synth.Inputs(inp.qkv[:, :s.T], inp.f[:, :s.T], inp.beta[:, :s.T], inp.z[:, :s.T])
-        self.case = dev.upload(s, params, first, state, device=device,
-                               hist=(op == gdn.OP_VERIFY))
+        self.case = dev.upload(s, params, first, state, device=device, hist=(mode == "verify"))
         self.out = torch.empty((n, s.B, s.T, s.H_v * s.d_v), device=device)
         self.host_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         self.abi_shape = self.case.abi_shape()
@@ -320,15 +324,17 @@ class SingleLaunch(Workload):
         return self.gdn.tensors_from_torch(
             qkv=self.dev_in["qkv"][j], f=self.dev_in["f"][j], beta=self.dev_in["beta"][j],
             z=self.dev_in["z"][j], conv_w=c.conv_w, A_log=c.A_log, dt_bias=c.dt_bias,
-            norm_w=c.norm_w, conv_state=c.conv_state, state=c.state, out=self.out[j],
-            state_hist=c.state_hist)
+            norm_w=c.norm_w, conv_state=c.conv_state, state=c.state,
+            out=None if self.mode == "commit" else self.out[j], state_hist=c.state_hist)
 
     def _launch(self, j):
         import torch
         st = torch.cuda.current_stream().cuda_stream
         g = self.gdn
-        if self.op == g.OP_DECODE:
+        if self.mode == "decode":
             g.gdn_decode_step(self.abi_shape, self._tensors(j), st)
+        elif self.mode == "commit":
+            g.gdn_commit_accepted(self.abi_shape, self._tensors(j), None, st)
         elif self.op == g.OP_VERIFY:
             g.gdn_verify_T(self.abi_shape, self._tensors(j), st)
         else:
@@ -349,14 +355,23 @@ class SingleLaunch(Workload):
         self.host_out[j].copy_(self.out[j], non_blocking=True)
 
 
+# The verify workload's two calls of a speculative step without per-token states:
+# a verify that writes outputs only, then the in-place commit of the accepted tokens.
+EXTRA_WORKLOADS = {"kda_verify_b32_t4_outputs_only": ("kda_verify_b32_t4", "verify_outputs"),
+                   "kda_commit_b32_t4": ("kda_verify_b32_t4", "commit")}
+
+
 def make_workload(name, device):
     import linear_attention_decode_kda_gb300 as gdn
-    spec = synth.WORKLOADS[name]
+    spec = synth.WORKLOADS.get(name)
     if name == "kda_decode_b1_34layers":
         return DecodeLayers(name, spec, device)
-    op = {"kda_decode_b64": gdn.OP_DECODE, "kda_verify_b32_t4": gdn.OP_VERIFY,
-          "gdn_prefill_b4_t4096": gdn.OP_PREFILL, "tiny_gdn_decode": gdn.OP_DECODE}[name]
-    return SingleLaunch(name, spec, device, op)
+    if name in EXTRA_WORKLOADS:
+        base, mode = EXTRA_WORKLOADS[name]
+        return SingleLaunch(name, synth.WORKLOADS[base], device, mode)
+    mode = {"kda_decode_b64": "decode", "kda_verify_b32_t4": "verify",
+            "gdn_prefill_b4_t4096": "prefill", "tiny_gdn_decode": "decode"}[name]
+    return SingleLaunch(name, spec, device, mode)
 
 
 # ---------------------------------------------------------------- ranks
@@ -570,7 +585,8 @@ def run_ours(args):
 
     if rank == 0 and not args.no_workloads:
         extra = {}
-        for name in ("kda_decode_b64", "kda_verify_b32_t4", "gdn_prefill_b4_t4096"):
+        for name in ("kda_decode_b64", "kda_verify_b32_t4", "kda_verify_b32_t4_outputs_only",
+                     "kda_commit_b32_t4", "gdn_prefill_b4_t4096"):
             if name == main.name:
                 continue
             w = make_workload(name, device)

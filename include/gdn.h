@@ -114,7 +114,7 @@ typedef struct {
     float *conv_state;     /* [B,conv_K-1,C], oldest row first                    */
     float *state;          /* [B,H_v,d_k,d_v]; row = key channel                  */
     void *out;             /* [B,T,H_v*d_v] out_dtype                             */
-    float *state_hist;     /* verify: [T,B,H_v,d_k,d_v]; otherwise unused         */
+    float *state_hist;     /* verify: [T,B,H_v,d_k,d_v] or NULL; otherwise unused */
     float *conv_hist;      /* verify: [T,B,conv_K-1,C] or NULL; otherwise unused  */
 } gdn_tensors_t;
 
@@ -130,13 +130,31 @@ GDN_API gdn_status_t gdn_decode_step(const gdn_shape_t *shape, const gdn_tensors
  * Multi-token verify (1 <= T <= 4): steps 1-7 for tokens 0..T-1 in order, as T
  * decode steps would (the arithmetic per token is the decode step's, so the
  * outputs and per-token states equal T gdn_decode_step calls bit for bit).
- * state and conv_state are only read.  state_hist[t] receives the state after
- * token t; conv_hist[t], when not NULL, the conv window after token t.  To
- * commit k accepted tokens the caller adopts state_hist[k-1] and conv_hist[k-1]
- * ("opus_gdn_qsa" audit, the gdn_step commit / verify modes and history output).
+ * state and conv_state are only read.  state_hist[t], when not NULL, receives
+ * the state after token t; conv_hist[t], when not NULL, the conv window after
+ * token t.  With both NULL only out is written (the state is read once).  To
+ * commit k accepted tokens the caller either adopts state_hist[k-1] and
+ * conv_hist[k-1] or calls gdn_commit_accepted ("opus_gdn_qsa" audit, the
+ * gdn_step commit / verify modes and history output).
  */
 GDN_API gdn_status_t gdn_verify_T(const gdn_shape_t *shape, const gdn_tensors_t *t,
                           gdn_stream_t stream);
+
+/*
+ * In-place commit of accepted tokens (1 <= T <= 4 rows per sequence in
+ * qkv/f/beta/z): sequence b takes its first accepted[b] tokens (clamped to
+ * 0..T; accepted == NULL takes all T) through steps 1-7, and state and
+ * conv_state are advanced in place to the state and window after them -- the
+ * values verify would have written to state_hist[k-1] and conv_hist[k-1], bit
+ * for bit, and k = 0 leaves the sequence untouched.  out may be NULL; when it
+ * is not, the rows of the taken tokens receive y and the other rows are left
+ * alone.  state_hist and conv_hist are ignored.  accepted is a device array
+ * of B int32 read by the kernel after its dependency wait, so the kernel
+ * queued before this call may write it ("opus_gdn_qsa" audit, the gdn_step
+ * commit modes: commit all, none, or the first k tokens).
+ */
+GDN_API gdn_status_t gdn_commit_accepted(const gdn_shape_t *shape, const gdn_tensors_t *t,
+                                 const int32_t *accepted, gdn_stream_t stream);
 
 /*
  * Chunked prefill of T >= 1 tokens per sequence: the same result as T decode

@@ -52,7 +52,7 @@ class GdnError(RuntimeError):
         self.status = status
 
 
-EXPORTS = ("gdn_decode_step", "gdn_verify_T", "gdn_prefill_chunked",
+EXPORTS = ("gdn_decode_step", "gdn_verify_T", "gdn_commit_accepted", "gdn_prefill_chunked",
            "gdn_prefill_workspace_bytes", "gdn_device_status", "gdn_status_string",
            "gdn_kernel_variant")
 
@@ -78,6 +78,8 @@ def load():
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = [S, Tn, P]
+    lib.gdn_commit_accepted.restype = ctypes.c_int
+    lib.gdn_commit_accepted.argtypes = [S, Tn, P, P]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked.argtypes = [S, Tn, P, ctypes.c_size_t, P]
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
@@ -109,6 +111,14 @@ def gdn_decode_step(shape: GdnShape, tensors: GdnTensors, stream: int = 0) -> No
 def gdn_verify_T(shape: GdnShape, tensors: GdnTensors, stream: int = 0) -> None:
     _check(load().gdn_verify_T(ctypes.byref(shape), ctypes.byref(tensors),
                                ctypes.c_void_p(stream)), "gdn_verify_T")
+
+
+def gdn_commit_accepted(shape: GdnShape, tensors: GdnTensors, accepted=None,
+                        stream: int = 0) -> None:
+    """accepted: device int32 [B] (a tensor or an address), or None for all T tokens."""
+    _check(load().gdn_commit_accepted(ctypes.byref(shape), ctypes.byref(tensors),
+                                      ctypes.c_void_p(_ptr(accepted)), ctypes.c_void_p(stream)),
+           "gdn_commit_accepted")
 
 
 def gdn_prefill_chunked(shape: GdnShape, tensors: GdnTensors, workspace: int = 0,

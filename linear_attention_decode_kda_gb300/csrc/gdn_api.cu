@@ -54,13 +54,15 @@ gdn_status_t check_shape(const gdn_shape_t *s)
 bool aligned(const void *p, unsigned bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
 
 // Vector-accessed buffers (state, conv_w, out) need 16 bytes; the rest their element size.
-gdn_status_t check_tensors(const gdn_shape_t *s, const gdn_tensors_t *t)
+// `out` may be NULL only where the entry point allows it.
+gdn_status_t check_tensors(const gdn_shape_t *s, const gdn_tensors_t *t, bool out_optional = false)
 {
     if (!t) return GDN_ERR_NULL;
     const void *req[] = {t->qkv, t->f, t->beta, t->z, t->conv_w, t->A_log, t->dt_bias,
-                         t->norm_w, t->conv_state, t->state, t->out};
+                         t->norm_w, t->conv_state, t->state};
     for (const void *p : req)
         if (!p) return GDN_ERR_NULL;
+    if (!t->out && !out_optional) return GDN_ERR_NULL;
     const unsigned ib = s->in_dtype == GDN_BF16 ? 2u : 4u;
     if (!aligned(t->qkv, ib) || !aligned(t->f, ib) || !aligned(t->beta, ib) ||
         !aligned(t->z, ib) || !aligned(t->A_log, 4) || !aligned(t->dt_bias, 4) ||
@@ -142,8 +144,7 @@ gdn_status_t gdn_verify_T(const gdn_shape_t *s, const gdn_tensors_t *t, gdn_stre
     if (s->T < 1 || s->T > 4) return GDN_ERR_SHAPE;
     rc = check_tensors(s, t);
     if (rc != GDN_OK) return rc;
-    if (!t->state_hist) return GDN_ERR_NULL;
-    if (!aligned16(t->state_hist) || (t->conv_hist && !aligned(t->conv_hist, 4)))
+    if ((t->state_hist && !aligned16(t->state_hist)) || (t->conv_hist && !aligned(t->conv_hist, 4)))
         return GDN_ERR_ALIGN;
     gdn::StepPlan plan;
     if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
@@ -151,6 +152,25 @@ gdn_status_t gdn_verify_T(const gdn_shape_t *s, const gdn_tensors_t *t, gdn_stre
     gdn::StepArgs a = step_args(s, t);
     a.state_hist = t->state_hist;
     a.conv_hist = t->conv_hist;
+    return run_step(s, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_commit_accepted(const gdn_shape_t *s, const gdn_tensors_t *t, const int32_t *accepted,
+                                 gdn_stream_t stream)
+{
+    gdn_status_t rc = check_shape(s);
+    if (rc != GDN_OK) return rc;
+    if (s->T < 1 || s->T > 4) return GDN_ERR_SHAPE;
+    rc = check_tensors(s, t, true);
+    if (rc != GDN_OK) return rc;
+    if (accepted && !aligned(accepted, 4)) return GDN_ERR_ALIGN;
+    gdn::StepPlan plan;
+    if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (s->B == 0) return GDN_OK;
+    gdn::StepArgs a = step_args(s, t);
+    a.state_out = t->state;
+    a.conv_out = t->conv_state;
+    a.accepted = accepted;
     return run_step(s, a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -15,9 +15,10 @@ struct StepArgs {
     float *state_out;            // commit: final state (may equal state_in); else NULL
     const float *conv_in;        // [B,K-1,C] conv window read at the first token
     float *conv_out;             // commit: final window (may equal conv_in); else NULL
-    void *out;                   // [B,T,H_v,D]
+    void *out;                   // [B,T,H_v,D], or NULL (commit without outputs)
     float *state_hist;           // [T,B,H_v,D,D] or NULL
     float *conv_hist;            // [T,B,K-1,C] or NULL
+    const int32_t *accepted;     // [B]: tokens taken per sequence (clamped to 0..T), or NULL for T
     int B, T, H_qk, H_v, C;
     int group;                   // H_v / H_qk
     int kda, in_bf16, out_bf16;

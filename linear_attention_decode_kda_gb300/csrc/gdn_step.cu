@@ -169,13 +169,16 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     };
 
     TokenIn<CQ, CV> cur;
-    load_token(0, cur);
+    // tokens taken for this sequence: all T, or the caller's accepted count
+    const int Tb = a.accepted ? min(max(a.accepted[b], 0), a.T) : a.T;
+    if (Tb > 0) load_token(0, cur);
+    if (clustered) cluster_wait_acquire();  // every CTA of the cluster has set up its barriers
 
 #pragma unroll 1
-    for (int t = 0; t < a.T; ++t) {
+    for (int t = 0; t < Tb; ++t) {
         if (t > 0) __syncthreads();  // previous token's shared-memory reads are done
         TokenIn<CQ, CV> nxt;
-        if (t + 1 < a.T) load_token(t + 1, nxt);
+        if (t + 1 < Tb) load_token(t + 1, nxt);
         const size_t bth = (static_cast<size_t>(b) * a.T + t) * a.H_v + h;
 
         // 1. conv + SiLU, norms' partial sums, gates
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         }
 
         // 4. state update and stores (they do not wait for the RMS exchange)
-        const bool last = (t == a.T - 1);
+        const bool last = (t == Tb - 1);
         float *hist = a.state_hist
             ? a.state_hist + ((static_cast<size_t>(t) * a.B + b) * a.H_v + h) * D * D + col0
             : nullptr;
@@ -310,7 +313,6 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         }
         float total = p;
         if (clustered) {
-            if (t == 0) cluster_wait_acquire();  // every CTA of the cluster has set up its barriers
             if (tid == 0) {
                 mbar_expect_tx(&rms_bar[t & 1], NSLAB * 4);
 #pragma unroll
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
                 for (int s = 0; s < NSLAB; ++s) total += rms_slot[t & 1][s];
             }
         }
-        if (rg == 0) {
+        if (rg == 0 && a.out) {
             const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
             float y[4];
 #pragma unroll
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         }
     }
     if (!ok) atomicOr(&g_step_error, 1u);
-    if (a.conv_out) {
+    if (a.conv_out && Tb > 0) {
         float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
 #pragma unroll
         for (int m = 0; m < CQ; ++m) {

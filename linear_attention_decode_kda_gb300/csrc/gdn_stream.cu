@@ -197,6 +197,12 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
         }
     }
 
+    // tokens taken per sequence: all T, or the caller's accepted count (read one head ahead)
+    auto tokens_of = [&](int j) {
+        return a.accepted ? min(max(a.accepted[j / a.H_v], 0), T) : T;
+    };
+    int tb_next = c0 < n_heads ? tokens_of(c0) : 0;
+
     bool ok = true;
     int tok = 0;  // tokens processed by this CTA: parity selects the partial-sum buffer
     int k = 0;
@@ -204,6 +210,8 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
     for (int j = c0; j < n_heads; j += G, ++k) {
         const int is = k % nst, hp = k & 1;
         const int b = j / a.H_v, h = j % a.H_v;
+        const int Tb = tb_next;  // tokens of this head
+        if (j + G < n_heads) tb_next = tokens_of(j + G);
         char *in = ins + is * L.bytes;
         // Several tokens per head: the previous head's readers of the per-token
         // rows are done before they are overwritten.  One token: slots alternate.
@@ -228,7 +236,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
             const float dt = qk_thr ? (a.kda ? 0.0f : reinterpret_cast<const float *>(in + L.dt)[h & 3])
                                     : (a.kda ? reinterpret_cast<const float *>(in + L.dt)[ch] : 0.0f);
 #pragma unroll 1
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t < Tb; ++t) {
                 const int sl = T > 1 ? t : hp;
                 const char *qkv = in + L.qkv + t * 3 * SD * es;
                 if (qk_thr) {
@@ -275,7 +283,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
                     }
                 }
             }
-            if (a.conv_out) {  // the window after the last token
+            if (a.conv_out && Tb > 0) {  // the window after the last token
                 float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
 #pragma unroll
                 for (int r = 0; r < KM1; ++r) {
@@ -309,7 +317,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
         }
 
 #pragma unroll 1
-        for (int t = 0; t < T; ++t, ++tok) {
+        for (int t = 0; t < Tb; ++t, ++tok) {
             const int sl = T > 1 ? t : hp;
             float *red_k = red + (n_red(T) > 1 ? (tok & 1) : 0) * 2 * CW * SD;
             float *red_q = red_k + CW * SD;
@@ -374,7 +382,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
             for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
 
             // gated RMSNorm output, written by one warp per token
-            if (warp == (t & (CW - 1))) {
+            if (a.out && warp == (t & (CW - 1))) {
                 const float rinv = 1.0f / sqrtf(p / static_cast<float>(SD) + a.eps_norm);
                 const float4 g4 = *reinterpret_cast<const float4 *>(&sh.gz[sl][col0]);
                 store_out4(a.out, e * SD + col0, a.out_bf16, o4.x * rinv * g4.x, o4.y * rinv * g4.y,
@@ -399,7 +407,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
             float *dst = nullptr;
             if (a.state_hist)
                 dst = a.state_hist + ((static_cast<size_t>(t) * a.B + b) * a.H_v + h) * SD * SD;
-            else if (a.state_out && t == T - 1)
+            else if (a.state_out && t == Tb - 1)
                 dst = a.state_out + static_cast<size_t>(j) * SD * SD;
             if (dst) {
 #pragma unroll

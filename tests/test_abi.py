@@ -99,8 +99,23 @@ def test_token_counts(lib):
     assert _call(lib, "verify", _shape(T=0), _tensors()) == gdn.GDN_ERR_SHAPE
     assert _call(lib, "prefill", _shape(T=0), _tensors()) == gdn.GDN_ERR_SHAPE
     t = _tensors()
-    t.state_hist = None
-    assert _call(lib, "verify", _shape(T=2), t) == gdn.GDN_ERR_NULL
+    t.state_hist = t.state_hist + 4
+    assert _call(lib, "verify", _shape(T=2), t) == gdn.GDN_ERR_ALIGN
+
+
+def test_commit_accepted_checks(lib):
+    def commit(shape, tensors, accepted=None):
+        return lib.gdn_commit_accepted(ctypes.byref(shape), ctypes.byref(tensors), accepted, None)
+    assert commit(_shape(T=0), _tensors()) == gdn.GDN_ERR_SHAPE
+    assert commit(_shape(T=5), _tensors()) == gdn.GDN_ERR_SHAPE
+    t = _tensors()
+    t.qkv = None
+    assert commit(_shape(T=2), t) == gdn.GDN_ERR_NULL
+    assert commit(_shape(T=2), _tensors(), 0x20002) == gdn.GDN_ERR_ALIGN
+    t = _tensors()
+    t.out = t.out + 8
+    assert commit(_shape(T=2), t) == gdn.GDN_ERR_ALIGN
+    assert lib.gdn_commit_accepted(None, ctypes.byref(_tensors()), None, None) == gdn.GDN_ERR_NULL
 
 
 def test_prefill_workspace_checks(lib):
