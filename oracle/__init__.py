@@ -38,7 +38,8 @@ def build(src: str = _SRC, out: str = _LIB, extra=()) -> str:
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H_qk", ctypes.c_int),
                 ("H_v", ctypes.c_int), ("d_k", ctypes.c_int), ("d_v", ctypes.c_int),
-                ("K", ctypes.c_int), ("kda", ctypes.c_int), ("q_scale", ctypes.c_double),
+                ("K", ctypes.c_int), ("gate", ctypes.c_int), ("out_gate", ctypes.c_int),
+                ("q_scale", ctypes.c_double),
                 ("eps_l2", ctypes.c_double), ("eps_norm", ctypes.c_double)]
 
 
@@ -62,7 +63,9 @@ def load(path: Optional[str] = None):
     lib.gdn_oracle_log_decay.argtypes = [ctypes.c_int, _P, _P, ctypes.c_double, _P]
     lib.gdn_oracle_delta_step.argtypes = [ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_double,
                                           _P, _P, _P, _P]
-    lib.gdn_oracle_gated_rmsnorm.argtypes = [ctypes.c_int, _P, _P, _P, ctypes.c_double, _P]
+    lib.gdn_oracle_log_decay_lb.argtypes = [ctypes.c_int, _P, ctypes.c_double, ctypes.c_double, _P]
+    lib.gdn_oracle_gated_rmsnorm.argtypes = [ctypes.c_int, _P, _P, _P, ctypes.c_double, ctypes.c_int,
+                                             _P]
     lib.gdn_oracle_conv.argtypes = [ctypes.POINTER(Shape), _P, _P, _P, _P]
     lib.gdn_oracle_run.restype = ctypes.c_int
     lib.gdn_oracle_run.argtypes = [ctypes.POINTER(Shape)] + [_P] * 13 + [ctypes.c_int]
@@ -87,8 +90,11 @@ def _f64(a) -> np.ndarray:
 
 def make_shape(shape) -> Shape:
     """ctypes shape from any object with the synth.Shape fields."""
+    lb = getattr(shape, "lb_gate", False)
+    gate = 2 if lb else (1 if shape.kda else 0)
+    out_gate = 1 if getattr(shape, "sigmoid_out", False) else 0
     return Shape(shape.B, shape.T, shape.H_qk, shape.H_v, shape.d_k, shape.d_v, shape.K,
-                 1 if shape.kda else 0, shape.q_scale, shape.eps_l2, shape.eps_norm)
+                 gate, out_gate, shape.q_scale, shape.eps_l2, shape.eps_norm)
 
 
 def run(shape, params, inputs, conv_state, state, *, hist: bool = False, o_raw: bool = False,
@@ -182,9 +188,18 @@ def log_decay(f, dt_bias, A_log, lib=None):
     return g
 
 
-def gated_rmsnorm(o, z, w, eps, lib=None):
+def log_decay_lb(f, a, lb, lib=None):
+    lib = lib or load()
+    f = _f64(f)
+    g = np.empty_like(f)
+    lib.gdn_oracle_log_decay_lb(f.size, _ptr(f), float(a), float(lb), _ptr(g))
+    return g
+
+
+def gated_rmsnorm(o, z, w, eps, sigmoid_gate: bool = False, lib=None):
     lib = lib or load()
     o, z, w = _f64(o), _f64(z), _f64(w)
     y = np.empty_like(o)
-    lib.gdn_oracle_gated_rmsnorm(o.size, _ptr(o), _ptr(z), _ptr(w), float(eps), _ptr(y))
+    lib.gdn_oracle_gated_rmsnorm(o.size, _ptr(o), _ptr(z), _ptr(w), float(eps),
+                                 1 if sigmoid_gate else 0, _ptr(y))
     return y

@@ -15,12 +15,15 @@
  *   a2  split xhat into q [H_qk,d_k], k [H_qk,d_k], v [H_v,d_v];
  *       q <- q * s / sqrt(sum q^2 + eps_l2),  k <- k / sqrt(sum k^2 + eps_l2)
  *   a3  g = -exp(A_log[h]) * softplus(f + dt_bias)   (per key channel: KDA;
- *       one per head: GDN);  alpha = exp(g)
+ *       one per head: GDN);  alpha = exp(g).  Lower-bound ("safe") gate of the
+ *       GLM KDA ("llama.cpp PR #84", the KDA decay precompute):
+ *       g = lb[h] * sigmoid(-a[h] f) per key channel, lb <= 0 bounding g from below
  *   a4  beta = sigmoid(beta_logit)
  *   a5  S <- (I - beta k k^T) Diag(alpha) S + beta k v^T, written as
  *       St = Diag(alpha) S;  u = beta (v - St^T k);  S = St + k u^T
  *   a6  o = S^T q (with the updated S)
- *   a7  y = o / sqrt(mean(o^2) + eps_norm) * w * silu(z)
+ *   a7  y = o / sqrt(mean(o^2) + eps_norm) * w * silu(z)   (or * sigmoid(z), the
+ *       output gate of the GLM KDA: "llama.cpp PR #84", the gated-norm fusion)
  *
  * Readings where the pages are silent (listed with the other readings in the
  * design notes): softplus(x) = max(x,0) + log1p(exp(-|x|)) with no cut-off;
@@ -39,7 +42,9 @@
 
 typedef struct {
     int B, T, H_qk, H_v, d_k, d_v, K;
-    int kda;          /* 1: one decay per key channel (KDA); 0: one per head (GDN) */
+    int gate;         /* 0: one decay per head (GDN); 1: per key channel (KDA);
+                         2: per key channel, lower-bound form (A_log holds a, dt_bias lb) */
+    int out_gate;     /* 0: silu(z); 1: sigmoid(z) */
     double q_scale;   /* d_k^-1/2 as the caller rounded it */
     double eps_l2, eps_norm;
 } gdn_oracle_shape;
@@ -76,6 +81,12 @@ void gdn_oracle_log_decay(int n, const double *f, const double *dt_bias, double 
     for (int i = 0; i < n; ++i) g[i] = -a * gdn_oracle_softplus(f[i] + dt_bias[i]);
 }
 
+/* Lower-bound log-decay g[i] = lb * sigmoid(-a * f[i]) for n channels. */
+void gdn_oracle_log_decay_lb(int n, const double *f, double a, double lb, double *g)
+{
+    for (int i = 0; i < n; ++i) g[i] = lb * gdn_oracle_sigmoid(-a * f[i]);
+}
+
 /* ---------------------------------------------------------------- a5 + a6 */
 
 /*
@@ -105,14 +116,16 @@ void gdn_oracle_delta_step(int d_k, int d_v, double *S, const double *alpha, dou
 
 /* ---------------------------------------------------------------- a7 */
 
+/* sigmoid_gate: 0 multiplies by silu(z), 1 by sigmoid(z). */
 void gdn_oracle_gated_rmsnorm(int n, const double *o, const double *z, const double *w,
-                              double eps, double *y)
+                              double eps, int sigmoid_gate, double *y)
 {
     double ms = 0.0;
     for (int j = 0; j < n; ++j) ms += o[j] * o[j];
     ms /= (double)n;
     double r = 1.0 / sqrt(ms + eps);
-    for (int j = 0; j < n; ++j) y[j] = o[j] * r * w[j] * gdn_oracle_silu(z[j]);
+    for (int j = 0; j < n; ++j)
+        y[j] = o[j] * r * w[j] * (sigmoid_gate ? gdn_oracle_sigmoid(z[j]) : gdn_oracle_silu(z[j]));
 }
 
 /* ---------------------------------------------------------------- a1 */
@@ -195,7 +208,12 @@ static void token_inputs(const job_t *J, int b, int h, int t, double *q, double 
         v[j] = conv_at(s, J->qkv, J->conv_w, J->conv_state0, b, t, voff + j);
 
     size_t bth = ((size_t)b * s->T + t) * s->H_v + h;
-    if (s->kda) {
+    if (s->gate == 2) {
+        double *fi = (double *)malloc(sizeof(double) * (size_t)s->d_k);
+        for (int i = 0; i < s->d_k; ++i) fi[i] = (double)J->f[bth * s->d_k + i];
+        gdn_oracle_log_decay_lb(s->d_k, fi, (double)J->A_log[h], (double)J->dt_bias[h], g);
+        free(fi);
+    } else if (s->gate == 1) {
         double *fi = (double *)malloc(sizeof(double) * (size_t)s->d_k);
         double *di = (double *)malloc(sizeof(double) * (size_t)s->d_k);
         for (int i = 0; i < s->d_k; ++i) {
@@ -224,7 +242,7 @@ static void emit_output(const job_t *J, int b, int h, int t, const double *o)
         z[j] = (double)J->z[row + j];
         w[j] = (double)J->norm_w[j];
     }
-    gdn_oracle_gated_rmsnorm(s->d_v, o, z, w, s->eps_norm, J->y + row);
+    gdn_oracle_gated_rmsnorm(s->d_v, o, z, w, s->eps_norm, s->out_gate, J->y + row);
     if (J->o_raw) memcpy(J->o_raw + row, o, sizeof(double) * (size_t)s->d_v);
     free(z);
     free(w);

@@ -108,7 +108,9 @@ class Shape:
     B sequences, T tokens per call, H_qk query/key heads, H_v value heads,
     d_k / d_v head widths, K conv taps.  ``kda`` selects the per-key-channel
     decay (Kimi Delta Attention); otherwise the decay is one scalar per head
-    (Gated DeltaNet).  ``bf16_in`` stores q/k/v/f/beta/z as bf16.
+    (Gated DeltaNet).  ``lb_gate`` (with ``kda``) selects the lower-bound form
+    of the per-channel decay, ``sigmoid_out`` the sigmoid output gate.
+    ``bf16_in`` stores q/k/v/f/beta/z as bf16.
     """
     B: int
     T: int
@@ -122,6 +124,8 @@ class Shape:
     chunk: int = 64
     eps_l2: float = 1e-6
     eps_norm: float = 1e-6
+    lb_gate: bool = False
+    sigmoid_out: bool = False
 
     @property
     def C(self) -> int:
@@ -190,16 +194,23 @@ def _f32(x: np.ndarray, shape) -> np.ndarray:
 def make_params(shape: Shape, seed: int = 0, layer: int = 0, slow_decay: bool = False) -> Params:
     s = shape
     conv_w = _f32(0.25 * normal(stream_key(seed, "conv_w", layer), s.C * s.K), (s.C, s.K))
-    if slow_decay:
-        # exp(A_log) in [0.02, 0.1]: with softplus of O(1) the log-decay is |g| <~ 0.1.
-        A_log = _f32(uniform(stream_key(seed, "A_log_slow", layer), s.H_v,
-                             math.log(0.02), math.log(0.1)), (s.H_v,))
+    if s.lb_gate:
+        # lower-bound gate g = lb * sigmoid(-a f): the per-head scale a in A_log's place,
+        # the bound lb <= 0 in dt_bias's (slow decay: a small bound)
+        A_log = _f32(uniform(stream_key(seed, "lb_a", layer), s.H_v, 0.5, 2.0), (s.H_v,))
+        lo, hi = (-0.2, -0.02) if slow_decay else (-4.0, -0.5)
+        dt_bias = _f32(uniform(stream_key(seed, "lb_bound", layer), s.H_v, lo, hi), (s.H_v,))
     else:
-        A_log = _f32(uniform(stream_key(seed, "A_log", layer), s.H_v, 0.0, math.log(16.0)),
-                     (s.H_v,))
-    dt_shape = (s.H_v, s.d_k) if s.kda else (s.H_v,)
-    dt_bias = _f32(0.5 * normal(stream_key(seed, "dt_bias", layer), int(np.prod(dt_shape))),
-                   dt_shape)
+        if slow_decay:
+            # exp(A_log) in [0.02, 0.1]: with softplus of O(1) the log-decay is |g| <~ 0.1.
+            A_log = _f32(uniform(stream_key(seed, "A_log_slow", layer), s.H_v,
+                                 math.log(0.02), math.log(0.1)), (s.H_v,))
+        else:
+            A_log = _f32(uniform(stream_key(seed, "A_log", layer), s.H_v, 0.0, math.log(16.0)),
+                         (s.H_v,))
+        dt_shape = (s.H_v, s.d_k) if s.kda else (s.H_v,)
+        dt_bias = _f32(0.5 * normal(stream_key(seed, "dt_bias", layer), int(np.prod(dt_shape))),
+                       dt_shape)
     norm_w = _f32(1.0 + 0.1 * normal(stream_key(seed, "norm_w", layer), s.d_v), (s.d_v,))
     return Params(conv_w, A_log, dt_bias, norm_w)
 

@@ -93,6 +93,22 @@ def pin_log_decay(lib):
     _close(g, [-120.0], rtol=1e-15, what="softplus(x) ~ x for large x")
 
 
+def pin_log_decay_lb(lib):
+    """Lower-bound gate g = lb sigmoid(-a f): closed forms and limits."""
+    g = oracle.log_decay_lb([0.0, 0.0], 1.7, -3.0, lib=lib)
+    _close(g, [-1.5, -1.5], what="f = 0 gives lb / 2")
+    g = oracle.log_decay_lb([math.log(3.0)], 1.0, -2.0, lib=lib)
+    _close(g, [-0.5], what="sigmoid(-ln 3) = 1/4")
+    f = np.array([0.3, -1.2, 2.5])
+    _close(oracle.log_decay_lb(f, 0.8, -1.6, lib=lib) + oracle.log_decay_lb(-f, 0.8, -1.6, lib=lib),
+           np.full(3, -1.6), what="g(f) + g(-f) = lb")
+    _close(oracle.log_decay_lb(f, 2.0, -1.6, lib=lib), oracle.log_decay_lb(2.0 * f, 1.0, -1.6, lib=lib),
+           what="a scales f")
+    g = oracle.log_decay_lb([800.0, -800.0], 1.0, -2.5, lib=lib)
+    _close(np.exp(g), [1.0, math.exp(-2.5)], atol=0.0, rtol=1e-15,
+           what="alpha -> 1 for large a f, exp(lb) for large -a f")
+
+
 # ---------------------------------------------------------------- a5 + a6
 
 def pin_delta_identity(lib):
@@ -164,6 +180,21 @@ def pin_gated_rmsnorm(lib):
     # eps under the root: mean(o^2) = 4/16, eps = 3/4 -> rms 1
     y = oracle.gated_rmsnorm(e, np.full(16, 50.0), np.ones(16), 0.75, lib=lib)
     _close(y[5], -2.0 * _silu(50.0), what="rmsnorm eps")
+
+
+def pin_gated_rmsnorm_sigmoid(lib):
+    """Sigmoid output gate: z = 0 halves, and y(z) / y(-z) = e^z."""
+    rng = np.random.default_rng(16)
+    o, w = rng.normal(size=8), rng.normal(size=8)
+    half = oracle.gated_rmsnorm(o, np.zeros(8), w, 0.0, sigmoid_gate=True, lib=lib)
+    r = 1.0 / np.sqrt(np.mean(o ** 2))
+    _close(half, 0.5 * o * r * w, what="sigmoid(0) = 1/2")
+    z = rng.normal(size=8)
+    yp = oracle.gated_rmsnorm(o, z, w, 0.0, sigmoid_gate=True, lib=lib)
+    ym = oracle.gated_rmsnorm(o, -z, w, 0.0, sigmoid_gate=True, lib=lib)
+    _close(yp / ym, np.exp(z), what="sigmoid(z) / sigmoid(-z) = e^z")
+    y3 = oracle.gated_rmsnorm(o, np.full(8, math.log(3.0)), w, 0.0, sigmoid_gate=True, lib=lib)
+    _close(y3, 0.75 * o * r * w, what="sigmoid(ln 3) = 3/4")
 
 
 # ---------------------------------------------------------------- a1
@@ -248,18 +279,20 @@ def pin_run_write_then_read(lib):
 
 
 def pin_run_decay_only(lib):
-    """beta = 0: S_t = Diag(prod alpha) S0 with alpha = exp(-exp(A_log) softplus(f + dt_bias))."""
-    for kda in (True, False):
+    """beta = 0: S_t = Diag(prod alpha) S0 with alpha = exp(-exp(A_log) softplus(f + dt_bias)),
+    or alpha = exp(lb sigmoid(-a f)) for the lower-bound gate (a in A_log, lb in dt_bias)."""
+    for kda, lb in ((True, False), (False, False), (True, True)):
         sh = synth.Shape(B=2, T=3, H_qk=1, H_v=2, d_k=4, d_v=3, K=4, kda=kda, bf16_in=False,
-                         eps_l2=0.0, eps_norm=1e-6)
+                         eps_l2=0.0, eps_norm=1e-6, lb_gate=lb)
         rng = np.random.default_rng(9)
         qkv = rng.normal(size=(sh.B, sh.T, sh.C)).astype(np.float32)
         f = rng.normal(size=(sh.B, sh.T, sh.H_v, sh.f_width)).astype(np.float32)
         inp = synth.Inputs(qkv=qkv, f=f,
                            beta=np.full((sh.B, sh.T, sh.H_v), -800.0, np.float32),
                            z=rng.normal(size=(sh.B, sh.T, sh.H_v, sh.d_v)).astype(np.float32))
-        A_log = np.array([0.3, -0.4], np.float32)
-        dt = rng.normal(size=(sh.H_v, sh.d_k) if kda else (sh.H_v,)).astype(np.float32)
+        A_log = np.array([0.3, -0.4], np.float32) if not lb else np.array([1.5, 0.7], np.float32)
+        dt = (rng.normal(size=(sh.H_v, sh.d_k) if kda else (sh.H_v,)).astype(np.float32)
+              if not lb else np.array([-2.0, -0.6], np.float32))
         prm = _identity_conv_params(sh, A_log, dt)
         cs0 = np.zeros((sh.B, sh.K - 1, sh.C), np.float32)
         S0 = rng.normal(size=(sh.B, sh.H_v, sh.d_k, sh.d_v)).astype(np.float32)
@@ -272,8 +305,11 @@ def pin_run_decay_only(lib):
                 for t in range(sh.T):
                     fb = f[b, t, h].astype(np.float64)
                     dth = dt[h].astype(np.float64)
-                    sp = np.logaddexp(0.0, fb + dth)            # softplus, library form
-                    a = np.exp(-math.exp(float(A_log[h])) * sp)
+                    if lb:
+                        a = np.exp(dth * (1.0 / (1.0 + np.exp(float(A_log[h]) * fb))))
+                    else:
+                        sp = np.logaddexp(0.0, fb + dth)            # softplus, library form
+                        a = np.exp(-math.exp(float(A_log[h])) * sp)
                     a = np.broadcast_to(a, (sh.d_k,))
                     S = a[:, None] * S
                     q = x[b, t, cq] * sh.q_scale / np.linalg.norm(x[b, t, cq])
@@ -364,7 +400,8 @@ def pin_head_permutation(lib):
     _close(out["state"], base["state"][:, p], rtol=0, atol=0, what="permuted state")
 
 
-ALL_PINS = [pin_scalars, pin_l2norm, pin_log_decay, pin_delta_identity, pin_delta_unit_key,
-            pin_delta_full_decay, pin_delta_bruteforce, pin_gated_rmsnorm, pin_conv,
+ALL_PINS = [pin_scalars, pin_l2norm, pin_log_decay, pin_log_decay_lb, pin_delta_identity,
+            pin_delta_unit_key, pin_delta_full_decay, pin_delta_bruteforce, pin_gated_rmsnorm,
+            pin_gated_rmsnorm_sigmoid, pin_conv,
             pin_run_write_then_read, pin_run_decay_only, pin_verify_equals_steps,
             pin_chunked_equals_sequential, pin_head_permutation]

@@ -27,8 +27,11 @@ MUTANTS = {
                            "(double)conv_w[c * s->K + (s->K - 1 - j)] *"),
     "q_scale_missing": ("gdn_oracle_l2norm(s->d_k, tmp, s->q_scale, s->eps_l2, q);",
                         "gdn_oracle_l2norm(s->d_k, tmp, 1.0, s->eps_l2, q);"),
-    "gate_silu_missing": ("y[j] = o[j] * r * w[j] * gdn_oracle_silu(z[j]);",
-                          "y[j] = o[j] * r * w[j] * z[j];"),
+    "gate_silu_missing": (": gdn_oracle_silu(z[j]));", ": z[j]);"),
+    "sigmoid_gate_is_silu": ("(sigmoid_gate ? gdn_oracle_sigmoid(z[j])", "(sigmoid_gate ? gdn_oracle_silu(z[j])"),
+    "lb_gate_sign": ("g[i] = lb * gdn_oracle_sigmoid(-a * f[i]);", "g[i] = lb * gdn_oracle_sigmoid(a * f[i]);"),
+    "lb_gate_uses_exp_a": ("g[i] = lb * gdn_oracle_sigmoid(-a * f[i]);",
+                           "g[i] = lb * gdn_oracle_sigmoid(-exp(a) * f[i]);"),
     "softplus_first_order": ("log1p(exp(-fabs(x)))", "exp(-fabs(x))"),
     "gva_head_map": ("int hq = h / group;", "int hq = h % s->H_qk;"),
     "conv_state_off_by_one": ("x_row(s, qkv, cs0, b, s->T + r, c)",
