@@ -358,7 +358,10 @@ class SingleLaunch(Workload):
 # The verify workload's two calls of a speculative step without per-token states:
 # a verify that writes outputs only, then the in-place commit of the accepted tokens.
 EXTRA_WORKLOADS = {"kda_verify_b32_t4_outputs_only": ("kda_verify_b32_t4", "verify_outputs"),
-                   "kda_commit_b32_t4": ("kda_verify_b32_t4", "commit")}
+                   "kda_commit_b32_t4": ("kda_verify_b32_t4", "commit"),
+                   # batched decode with the bounded per-channel gate and the sigmoid output gate
+                   "kda_decode_b64_bounded_gate": ("kda_decode_b64", "decode")}
+EXTRA_SHAPES = {"kda_decode_b64_bounded_gate": dict(lb_gate=True, sigmoid_out=True)}
 
 
 def make_workload(name, device):
@@ -368,7 +371,10 @@ def make_workload(name, device):
         return DecodeLayers(name, spec, device)
     if name in EXTRA_WORKLOADS:
         base, mode = EXTRA_WORKLOADS[name]
-        return SingleLaunch(name, synth.WORKLOADS[base], device, mode)
+        spec = dict(synth.WORKLOADS[base])
+        if name in EXTRA_SHAPES:
+            spec["shape"] = dataclasses.replace(spec["shape"], **EXTRA_SHAPES[name])
+        return SingleLaunch(name, spec, device, mode)
     mode = {"kda_decode_b64": "decode", "kda_verify_b32_t4": "verify",
             "gdn_prefill_b4_t4096": "prefill", "tiny_gdn_decode": "decode"}[name]
     return SingleLaunch(name, spec, device, mode)
@@ -585,8 +591,8 @@ def run_ours(args):
 
     if rank == 0 and not args.no_workloads:
         extra = {}
-        for name in ("kda_decode_b64", "kda_verify_b32_t4", "kda_verify_b32_t4_outputs_only",
-                     "kda_commit_b32_t4", "gdn_prefill_b4_t4096"):
+        for name in ("kda_decode_b64", "kda_decode_b64_bounded_gate", "kda_verify_b32_t4",
+                     "kda_verify_b32_t4_outputs_only", "kda_commit_b32_t4", "gdn_prefill_b4_t4096"):
             if name == main.name:
                 continue
             w = make_workload(name, device)

@@ -11,11 +11,16 @@
  *      head, v of every value head); q <- q * q_scale / sqrt(|q|^2 + eps_l2),
  *      k <- k / sqrt(|k|^2 + eps_l2).  Value head h reads qk head h / (H_v/H_qk).
  *   3. g = -exp(A_log[h]) * softplus(f + dt_bias)  (per key channel for
- *      GDN_GATE_PER_CHANNEL, one per head for GDN_GATE_PER_HEAD); alpha = exp(g)
+ *      GDN_GATE_PER_CHANNEL, one per head for GDN_GATE_PER_HEAD), or
+ *      g = dt_bias[h] * sigmoid(-A_log[h] * f) per key channel for
+ *      GDN_GATE_LOWER_BOUND (the GLM KDA's bounded "safe" decay, "llama.cpp
+ *      PR #84", the KDA decay precompute); alpha = exp(g)
  *   4. beta = sigmoid(beta_logit)
  *   5. S <- (I - beta k k^T) Diag(alpha) S + beta k v^T     (S is [d_k, d_v], fp32)
  *   6. o = S^T q
- *   7. y = o / sqrt(mean(o^2) + eps_norm) * norm_w * silu(z)
+ *   7. y = o / sqrt(mean(o^2) + eps_norm) * norm_w * silu(z), or * sigmoid(z)
+ *      with GDN_FLAG_SIGMOID_GATE (the GLM KDA's output gate, "llama.cpp PR #84",
+ *      the gated-norm fusion)
  *
  * Ownership: the caller owns every buffer.  The library allocates nothing,
  * keeps no state between calls, makes no host<->device copy and never
@@ -62,7 +67,10 @@ typedef enum {
 
 typedef enum {
     GDN_GATE_PER_HEAD = 0,    /* Gated DeltaNet: f [B,T,H_v],     dt_bias [H_v]     */
-    GDN_GATE_PER_CHANNEL = 1  /* KDA:            f [B,T,H_v,d_k], dt_bias [H_v,d_k] */
+    GDN_GATE_PER_CHANNEL = 1, /* KDA:            f [B,T,H_v,d_k], dt_bias [H_v,d_k] */
+    GDN_GATE_LOWER_BOUND = 2  /* KDA, bounded:   f [B,T,H_v,d_k]; A_log [H_v] holds
+                                 the scale a (used as is), dt_bias [H_v] the bound
+                                 lb <= 0 of the log-decay                          */
 } gdn_gate_mode_t;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
@@ -78,7 +86,9 @@ enum {
      * previous layer of a model).  Inputs q/k/v/f/beta/z are read after the
      * wait.  Without this flag launches are plain stream-ordered.
      */
-    GDN_FLAG_PDL = 1
+    GDN_FLAG_PDL = 1,
+    /* Output gate sigmoid(z) in place of silu(z). */
+    GDN_FLAG_SIGMOID_GATE = 2
 };
 
 typedef struct {

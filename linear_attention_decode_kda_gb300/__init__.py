@@ -26,9 +26,11 @@ GDN_ERR_TIMEOUT = -7
 
 GDN_GATE_PER_HEAD = 0
 GDN_GATE_PER_CHANNEL = 1
+GDN_GATE_LOWER_BOUND = 2
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_FLAG_PDL = 1
+GDN_FLAG_SIGMOID_GATE = 2
 
 OP_DECODE, OP_VERIFY, OP_PREFILL = 0, 1, 2
 
@@ -145,12 +147,13 @@ def gdn_kernel_variant(shape: GdnShape, op: int) -> Optional[str]:
 def make_shape(B: int, T: int, H_qk: int, H_v: int, d_k: int, d_v: int, *, kda: bool,
                bf16_in: bool, bf16_out: bool = False, conv_K: int = 4, chunk: int = 64,
                q_scale: float, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
-               pdl: bool = False) -> GdnShape:
+               pdl: bool = False, lb_gate: bool = False, sigmoid_gate: bool = False) -> GdnShape:
+    """lb_gate (with kda): the lower-bound per-channel gate; sigmoid_gate: sigmoid output gate."""
+    gate = GDN_GATE_LOWER_BOUND if lb_gate else (GDN_GATE_PER_CHANNEL if kda else GDN_GATE_PER_HEAD)
+    flags = (GDN_FLAG_PDL if pdl else 0) | (GDN_FLAG_SIGMOID_GATE if sigmoid_gate else 0)
     return GdnShape(B=B, T=T, H_qk=H_qk, H_v=H_v, d_k=d_k, d_v=d_v, conv_K=conv_K, chunk=chunk,
-                    gate_mode=GDN_GATE_PER_CHANNEL if kda else GDN_GATE_PER_HEAD,
-                    in_dtype=GDN_BF16 if bf16_in else GDN_F32,
-                    out_dtype=GDN_BF16 if bf16_out else GDN_F32,
-                    flags=GDN_FLAG_PDL if pdl else 0,
+                    gate_mode=gate, in_dtype=GDN_BF16 if bf16_in else GDN_F32,
+                    out_dtype=GDN_BF16 if bf16_out else GDN_F32, flags=flags,
                     q_scale=q_scale, eps_l2=eps_l2, eps_norm=eps_norm)
 
 

@@ -36,12 +36,13 @@ gdn_status_t check_shape(const gdn_shape_t *s)
         return GDN_ERR_SHAPE;
     if (s->H_v % s->H_qk != 0) return GDN_ERR_SHAPE;
     if (s->B > 65535 || s->H_v > 65535) return GDN_ERR_SHAPE;
-    if (s->gate_mode != GDN_GATE_PER_HEAD && s->gate_mode != GDN_GATE_PER_CHANNEL)
+    if (s->gate_mode != GDN_GATE_PER_HEAD && s->gate_mode != GDN_GATE_PER_CHANNEL &&
+        s->gate_mode != GDN_GATE_LOWER_BOUND)
         return GDN_ERR_SHAPE;
     if ((s->in_dtype != GDN_F32 && s->in_dtype != GDN_BF16) ||
         (s->out_dtype != GDN_F32 && s->out_dtype != GDN_BF16))
         return GDN_ERR_SHAPE;
-    if (s->flags & ~GDN_FLAG_PDL) return GDN_ERR_SHAPE;
+    if (s->flags & ~(GDN_FLAG_PDL | GDN_FLAG_SIGMOID_GATE)) return GDN_ERR_SHAPE;
     if (!(s->q_scale > 0.0f) || !(s->eps_l2 >= 0.0f) || !(s->eps_norm >= 0.0f))
         return GDN_ERR_SHAPE;
     if (s->conv_K != 4) return GDN_ERR_UNSUPPORTED;
@@ -92,7 +93,9 @@ gdn::StepArgs step_args(const gdn_shape_t *s, const gdn_tensors_t *t)
     a.H_v = s->H_v;
     a.C = 2 * s->H_qk * s->d_k + s->H_v * s->d_v;
     a.group = s->H_v / s->H_qk;
-    a.kda = s->gate_mode == GDN_GATE_PER_CHANNEL;
+    a.kda = s->gate_mode != GDN_GATE_PER_HEAD;
+    a.lb_gate = s->gate_mode == GDN_GATE_LOWER_BOUND;
+    a.sig_gate = (s->flags & GDN_FLAG_SIGMOID_GATE) != 0;
     a.in_bf16 = s->in_dtype == GDN_BF16;
     a.out_bf16 = s->out_dtype == GDN_BF16;
     a.q_scale = s->q_scale;

@@ -21,7 +21,10 @@ struct StepArgs {
     const int32_t *accepted;     // [B]: tokens taken per sequence (clamped to 0..T), or NULL for T
     int B, T, H_qk, H_v, C;
     int group;                   // H_v / H_qk
-    int kda, in_bf16, out_bf16;
+    int kda;                     // one decay per key channel (both per-channel gate forms)
+    int lb_gate;                 // lower-bound gate: A_log = scale a, dt_bias[h] = bound lb
+    int sig_gate;                // output gate sigmoid(z) instead of silu(z)
+    int in_bf16, out_bf16;
     float q_scale, eps_l2, eps_norm;
 };
 

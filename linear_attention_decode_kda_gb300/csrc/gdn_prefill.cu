@@ -523,7 +523,8 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
             const int t = t_lo + i;
             if (t < n) {
                 const float zz = get_bf16(zs, t * PD * 2 + ch * 2);
-                const float y = o[i] * ps.rinv[t] * nw * silu_fast(zz);
+                const float gz = a.sig_gate ? __fdividef(1.0f, 1.0f + __expf(-zz)) : silu_fast(zz);
+                const float y = o[i] * ps.rinv[t] * nw * gz;
                 const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + ch;
                 if (a.out_bf16)
                     reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);

@@ -102,7 +102,9 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     float wq[CQ][KM1], wk[CQ][KM1], wv[CV][KM1];
     float4 cwq[CQ], cwk[CQ], cwv[CV];
     float dtb[CQ];
-    const float A = expf(a.A_log[h]);
+    // softplus gates: A = exp(A_log); lower-bound gate: A = the scale a, lbv = the bound
+    const float A = a.lb_gate ? a.A_log[h] : expf(a.A_log[h]);
+    const float lbv = a.lb_gate ? a.dt_bias[h] : 0.0f;
 #pragma unroll
     for (int m = 0; m < CQ; ++m) {
         const int i = tid + m * NT;
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             }
             cwq[m] = reinterpret_cast<const float4 *>(a.conv_w)[cq];
             cwk[m] = reinterpret_cast<const float4 *>(a.conv_w)[ck];
-            dtb[m] = a.kda ? a.dt_bias[static_cast<size_t>(h) * D + i] : 0.0f;
+            dtb[m] = a.kda && !a.lb_gate ? a.dt_bias[static_cast<size_t>(h) * D + i] : 0.0f;
         }
     }
 #pragma unroll
@@ -196,7 +198,9 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
                 sq = fmaf(q, q, sq);
                 sk = fmaf(k, k, sk);
                 sqk = fmaf(q, k, sqk);
-                if (a.kda) a_s[i] = expf(-A * softplus_f(cur.fq[m] + dtb[m]));
+                if (a.kda)
+                    a_s[i] = a.lb_gate ? expf(lbv * sigmoid_f(-A * cur.fq[m]))
+                                       : expf(-A * softplus_f(cur.fq[m] + dtb[m]));
             }
         }
 #pragma unroll
@@ -329,7 +333,8 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
             float y[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) y[c] = o[c] * rinv * nw[c] * silu_f(cur.z[c]);
+            for (int c = 0; c < 4; ++c)
+                y[c] = o[c] * rinv * nw[c] * (a.sig_gate ? sigmoid_f(cur.z[c]) : silu_f(cur.z[c]));
             store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
         }
 

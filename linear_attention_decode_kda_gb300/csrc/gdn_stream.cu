@@ -57,7 +57,8 @@ struct InLayout {
     int qkv, win, cw, f, z, beta, dt, alog, bytes;
 };
 
-__host__ __device__ __forceinline__ InLayout in_layout(int T, int es, int kda)
+// kda: gate rows per key channel; dtpc: dt_bias per key channel (the softplus KDA gate)
+__host__ __device__ __forceinline__ InLayout in_layout(int T, int es, int kda, int dtpc)
 {
     InLayout L;
     L.qkv = 0;                                      // [T][3][SD] inputs
@@ -67,16 +68,18 @@ __host__ __device__ __forceinline__ InLayout in_layout(int T, int es, int kda)
     L.z = L.f + up128(T * (kda ? SD * es : 16));    // [T][SD] inputs
     L.beta = L.z + up128(T * SD * es);              // [T][16 B]
     L.dt = L.beta + up128(T * 16);                  // [SD] fp32, or 16 B
-    L.alog = L.dt + up128(kda ? SD * 4 : 16);       // 16 B
+    L.alog = L.dt + up128(dtpc ? SD * 4 : 16);      // 16 B
     L.bytes = L.alog + 128;
     return L;
 }
 
-__host__ __device__ __forceinline__ uint32_t input_bytes(int T, int es, int kda)
+__host__ __device__ __forceinline__ uint32_t input_bytes(int T, int es, int kda, int dtpc)
 {
     return T * 3 * SD * es + KM1 * 3 * SD * 4 + 3 * SD * 16 + T * (kda ? SD * es : 16) +
-           T * SD * es + T * 16 + (kda ? SD * 4 : 16) + 16;
+           T * SD * es + T * 16 + (dtpc ? SD * 4 : 16) + 16;
 }
+
+__host__ __device__ __forceinline__ int dt_per_channel(const StepArgs &a) { return a.kda && !a.lb_gate; }
 
 // The tensor maps of the input bundle (kernel parameters).
 struct InMaps {
@@ -116,7 +119,7 @@ __device__ __forceinline__ void issue_inputs(const StepArgs &a, const InMaps &m,
 {
     const int b = j / a.H_v, h = j % a.H_v;
     const int es = a.in_bf16 ? 2 : 4, per16 = 16 / es;
-    if (lane == 0) mbar_expect_tx(bar, input_bytes(a.T, es, a.kda));
+    if (lane == 0) mbar_expect_tx(bar, input_bytes(a.T, es, a.kda, dt_per_channel(a)));
     __syncwarp();
     const int bt = b * a.T;
     switch (lane) {
@@ -135,7 +138,7 @@ __device__ __forceinline__ void issue_inputs(const StepArgs &a, const InMaps &m,
     case 4: tma_load_3d(stage + L.z, &m.z, 0, h, bt, bar); break;
     case 5: tma_load_2d(stage + L.beta, &m.beta, h & ~(per16 - 1), bt, bar); break;
     case 6:
-        if (a.kda) tma_load_1d(stage + L.dt, a.dt_bias + static_cast<size_t>(h) * SD, SD * 4, bar);
+        if (dt_per_channel(a)) tma_load_1d(stage + L.dt, a.dt_bias + static_cast<size_t>(h) * SD, SD * 4, bar);
         else tma_load_1d(stage + L.dt, a.dt_bias + (h & ~3), 16, bar);
         break;
     case 7: tma_load_1d(stage + L.alog, a.A_log + (h & ~3), 16, bar); break;
@@ -162,7 +165,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = gridDim.x, c0 = blockIdx.x;
     const int C = a.C, T = a.T, es = a.in_bf16 ? 2 : 4, per16 = 16 / es;
-    const InLayout L = in_layout(T, es, a.kda);
+    const InLayout L = in_layout(T, es, a.kda, dt_per_channel(a));
     float *red = reinterpret_cast<float *>(ins + nst * L.bytes);  // [n_red][2][CW][SD]
     const bool qk_thr = tid < SD;  // q_i, k_i of channel tid; threads SD..2SD-1: gate, v, z
     const int ch = tid & (SD - 1);
@@ -223,7 +226,9 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
         {
             const float *win = reinterpret_cast<const float *>(in + L.win);
             const float4 *cwv = reinterpret_cast<const float4 *>(in + L.cw);
-            const float A = expf(reinterpret_cast<const float *>(in + L.alog)[h & 3]);
+            // softplus gates: A = exp(A_log); lower-bound gate: A = the scale a
+            const float A_raw = reinterpret_cast<const float *>(in + L.alog)[h & 3];
+            const float A = a.lb_gate ? A_raw : expf(A_raw);
             const int seg = qk_thr ? 0 : 2;  // q (and k) or v channels
             float w0[KM1], w1[KM1];
 #pragma unroll
@@ -233,8 +238,10 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
             }
             const float4 cw0 = cwv[seg * SD + ch];
             const float4 cw1 = qk_thr ? cwv[SD + ch] : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float dt = qk_thr ? (a.kda ? 0.0f : reinterpret_cast<const float *>(in + L.dt)[h & 3])
-                                    : (a.kda ? reinterpret_cast<const float *>(in + L.dt)[ch] : 0.0f);
+            // dt_bias of this thread's gate: per channel (softplus KDA), per head (GDN), or the
+            // lower bound (per head) of the bounded gate
+            const float dt = dt_per_channel(a) ? (qk_thr ? 0.0f : reinterpret_cast<const float *>(in + L.dt)[ch])
+                                               : reinterpret_cast<const float *>(in + L.dt)[h & 3];
 #pragma unroll 1
             for (int t = 0; t < Tb; ++t) {
                 const int sl = T > 1 ? t : hp;
@@ -267,12 +274,15 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
                         sh.red3[sl][warp][2] = sqk;
                     }
                 } else {
-                    if (a.kda)
-                        sh.a[sl][ch] = expf(-A * softplus_f(smem_in(in + L.f + t * SD * es, ch, a.in_bf16) + dt));
+                    if (a.kda) {
+                        const float fv = smem_in(in + L.f + t * SD * es, ch, a.in_bf16);
+                        sh.a[sl][ch] = a.lb_gate ? expf(dt * sigmoid_f(-A * fv)) : expf(-A * softplus_f(fv + dt));
+                    }
                     const float xv = smem_in(qkv, 2 * SD + ch, a.in_bf16);
                     sh.v[sl][ch] = conv4_silu(cw0, w0, xv);
                     w0[0] = w0[1]; w0[1] = w0[2]; w0[2] = xv;
-                    sh.gz[sl][ch] = nw * silu_f(smem_in(in + L.z + t * SD * es, ch, a.in_bf16));
+                    const float zv = smem_in(in + L.z + t * SD * es, ch, a.in_bf16);
+                    sh.gz[sl][ch] = nw * (a.sig_gate ? sigmoid_f(zv) : silu_f(zv));
                 }
                 if (a.conv_hist) {  // the window after token t
                     float *chh = a.conv_hist + (static_cast<size_t>(t) * a.B + b) * KM1 * C;
@@ -423,7 +433,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int smem_bytes(int T, int es, int kda, int nst)
 {
-    return 128 + SH_BYTES + static_cast<int>(TILE_BYTES) + nst * in_layout(T, es, kda).bytes +
+    return 128 + SH_BYTES + static_cast<int>(TILE_BYTES) + nst * in_layout(T, es, kda, kda).bytes +
            n_red(T) * 2 * CW * SD * 4;
 }
 

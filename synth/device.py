@@ -55,7 +55,8 @@ class DeviceCase:
         s = self.shape
         return gdn.make_shape(s.B, s.T, s.H_qk, s.H_v, s.d_k, s.d_v, kda=s.kda,
                               bf16_in=s.bf16_in, bf16_out=bf16_out, conv_K=s.K, chunk=s.chunk,
-                              q_scale=s.q_scale, eps_l2=s.eps_l2, eps_norm=s.eps_norm, pdl=pdl)
+                              q_scale=s.q_scale, eps_l2=s.eps_l2, eps_norm=s.eps_norm, pdl=pdl,
+                              lb_gate=s.lb_gate, sigmoid_gate=s.sigmoid_out)
 
 
 def upload(shape: Shape, params: Params, inputs: Inputs, state: State, device="cuda",

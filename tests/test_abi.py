@@ -137,6 +137,15 @@ def test_status_strings(lib):
     assert "unknown" in gdn.status_string(-99)
 
 
+def test_gate_variants_are_accepted(lib):
+    s = _shape(B=64, H_qk=32, H_v=32)
+    s.gate_mode = gdn.GDN_GATE_LOWER_BOUND
+    s.flags = gdn.GDN_FLAG_SIGMOID_GATE | gdn.GDN_FLAG_PDL
+    assert gdn.gdn_kernel_variant(s, gdn.OP_DECODE) == "stream<128>"
+    s.T = 64  # the bounded per-channel gate has no chunked form: the recurrent kernel runs
+    assert not gdn.gdn_kernel_variant(s, gdn.OP_PREFILL).startswith("chunked")
+
+
 def test_variant_choice(lib):
     # B*H_v head units: enough for two CTAs per SM -> streaming CTAs; B=1 -> 16-column slabs
     assert gdn.gdn_kernel_variant(_shape(B=64, H_qk=32, H_v=32), gdn.OP_DECODE) == "stream<128>"
