@@ -38,6 +38,9 @@ struct StepPlan {
 // Column-slab kernel (gdn_step.cu): any unit count, d in {16, 32, 64, 128}.
 bool plan_slab(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
 cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
+// The slab plan for long token loops: as plan_slab, with fewer slabs until the grid is
+// resident at once.
+bool plan_slab_one_wave(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
 
 // Persistent TMA-pipelined kernel (gdn_stream.cu): d = 128, ungrouped heads,
 // at least two (sequence, head) units per SM.

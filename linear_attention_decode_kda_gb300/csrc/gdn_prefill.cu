@@ -642,9 +642,10 @@ const char *prefill_variant(const gdn_shape_t &s, int num_sms)
         (s.chunk == CH || s.chunk == 64) && s.H_v / s.H_qk <= 8)
         return "chunked<128,32>";
     StepPlan plan;
-    if (!plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms > 0 ? num_sms : 148, &plan))
-        return nullptr;
-    return plan.name;
+    const int sms = num_sms > 0 ? num_sms : 148;
+    const bool planned = s.T <= 4 ? plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, sms, &plan)
+                                  : plan_slab_one_wave(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, sms, &plan);
+    return planned ? plan.name : nullptr;
 }
 
 gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *, int num_sms,
@@ -654,8 +655,12 @@ gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *, int nu
         cudaError_t e = launch_chunked(a, stream);
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
+    // the recurrent kernel over all T tokens: short runs take the step plan, long ones the
+    // column-slab plan that is resident in one wave
     StepPlan plan;
-    if (!plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan)) return GDN_ERR_UNSUPPORTED;
+    const bool planned = s.T <= 4 ? plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan)
+                                  : plan_slab_one_wave(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan);
+    if (!planned) return GDN_ERR_UNSUPPORTED;
     cudaError_t e = launch_step(plan, a, (s.flags & GDN_FLAG_PDL) != 0, num_sms, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -454,6 +454,32 @@ bool plan_slab(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
     return true;
 }
 
+// Long token loops (prefill on this kernel) run as one wave: every CTA holds its state
+// slab for the whole sequence, so a grid larger than the GPU holds at once would run the
+// loop twice over.  Halve the slab count of the regular plan until the grid fits.
+bool plan_slab_one_wave(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
+{
+    if (!plan_slab(D, B, H_v, group, num_sms, plan)) return false;
+    const long units = static_cast<long>(B) * H_v;
+    while (plan->nslab > 1) {
+        const Variant *v = find_variant(plan->D, plan->W);
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v->fn, v->NT, 0) != cudaSuccess)
+            per_sm = 1;
+        if (units * plan->nslab <= static_cast<long>(per_sm) * num_sms) break;
+        const int nslab = plan->nslab / 2;
+        const Variant *w = find_variant(D, D / nslab);
+        if (!w) break;
+        plan->nslab = nslab;
+        plan->W = w->W;
+        plan->threads = w->NT;
+        plan->cluster = nslab * group;
+        plan->grid = static_cast<int>(units) * nslab;
+        plan->name = w->name;
+    }
+    return true;
+}
+
 cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
 {
     const Variant *v = find_variant(plan.D, plan.W);
