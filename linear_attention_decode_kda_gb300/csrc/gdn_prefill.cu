@@ -51,6 +51,7 @@ constexpr int SM_R4 = SM_R3 + 4 * CH * PD * 2;     // T [CH x CH]
 constexpr int SM_R5 = SM_R4 + CH * CH * 2;         // Gram f32 [2CH][2CH], A f32, T f32
 constexpr int GS = 2 * CH + 1;                     // padded row stride of the f32 Gram
 constexpr int SQS = PD + 1;                         // padded row stride of the o^2 scratch
+constexpr int YS = PD + 4;                          // row stride of the y staging rows (16-byte aligned)
 constexpr int SM_BYTES = SM_R5 + 2 * CH * GS * 4 + 2 * CH * CH * 4;
 // operand offsets inside the regions
 constexpr int OP_VB = 0, OP_KBG = 2 * PD * CH * 2;                  // R2 (first use)
@@ -517,22 +518,27 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
         }
         if (ok) ok = mbar_wait_bounded(&ps.z_full, z_ph);
         z_ph ^= 1u;
-        __syncthreads();
+        __syncthreads();  // the o^2 sums are read: the scratch takes y
+        // y, token-major in shared memory, then 128-bit stores of 4 channels of a token
+        float *ys = reinterpret_cast<float *>(r1);  // [CH][YS]
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int t = t_lo + i;
+            const float zz = get_bf16(zs, t * PD * 2 + ch * 2);
+            const float gz = a.sig_gate ? __fdividef(1.0f, 1.0f + __expf(-zz)) : silu_fast(zz);
+            ys[t * YS + ch] = o[i] * ps.rinv[t] * nw * gz;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k4 = 0; k4 < CH * PD / 4 / PT; ++k4) {
+            const int e = tid + PT * k4, t = e / (PD / 4), c4 = 4 * (e % (PD / 4));
             if (t < n) {
-                const float zz = get_bf16(zs, t * PD * 2 + ch * 2);
-                const float gz = a.sig_gate ? __fdividef(1.0f, 1.0f + __expf(-zz)) : silu_fast(zz);
-                const float y = o[i] * ps.rinv[t] * nw * gz;
-                const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + ch;
-                if (a.out_bf16)
-                    reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
-                else
-                    reinterpret_cast<float *>(a.out)[idx] = y;
+                const float4 y4 = *reinterpret_cast<const float4 *>(ys + t * YS + c4);
+                const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + c4;
+                store_out4(a.out, idx, a.out_bf16, y4.x, y4.y, y4.z, y4.w);
             }
         }
-        __syncthreads();  // the z stage is consumed
+        __syncthreads();  // the z stage and the scratch are consumed
         if (warp == 0 && c0 + CH < T) issue_z(c0 + CH);
 
         // P12: S^T -> split operand for the next chunk
