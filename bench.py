@@ -79,6 +79,22 @@ def prefill_flops(s: synth.Shape) -> float:
     return float(s.B * nch * (s.H_v * per_v + s.H_qk * per_qk))
 
 
+# fp32 FMA peak of the part: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (maximum SM
+# clock).  The two-kernel chunked prefill runs its products on these lanes.
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def kda_chunk_flops(s: synth.Shape, C: int = 16) -> float:
+    """fp32 FLOPs of the two-kernel chunked form at chunk C, per (sequence, value
+    head, chunk): W S, Q S and the state update (2 C d^2 each), A V_new (2 C^2 d),
+    the pair sums K K^T and Q K^T over the lower triangle (C^2 d each) and the
+    forward substitution on 2d columns (C^2 d each side)."""
+    d = s.d_k
+    nch = -(-s.T // C)
+    per = 3 * 2 * C * d * d + 2 * C * C * d + 2 * C * C * d + 2 * C * C * d
+    return float(s.B * s.H_v * nch * per)
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -314,6 +330,8 @@ class SingleLaunch(Workload):
         m = re.match(r"chunked<\d+,(\d+)>", self.kernel or "") if op == gdn.OP_PREFILL else None
         self.flops_per_launch = (prefill_flops(dataclasses.replace(s, chunk=int(m.group(1))))
                                  if m else 0.0)
+        m = re.match(r"kda_chunked<(\d+)>", self.kernel or "") if op == gdn.OP_PREFILL else None
+        self.alu_flops_per_launch = kda_chunk_flops(s, int(m.group(1))) if m else 0.0
         self.ws_bytes = gdn.gdn_prefill_workspace_bytes(self.abi_shape) if op == 2 else 0
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         self.h2d_bytes = sum(v[0].numel() * v.element_size() for v in self.dev_in.values())
@@ -360,8 +378,12 @@ class SingleLaunch(Workload):
 EXTRA_WORKLOADS = {"kda_verify_b32_t4_outputs_only": ("kda_verify_b32_t4", "verify_outputs"),
                    "kda_commit_b32_t4": ("kda_verify_b32_t4", "commit"),
                    # batched decode with the bounded per-channel gate and the sigmoid output gate
-                   "kda_decode_b64_bounded_gate": ("kda_decode_b64", "decode")}
-EXTRA_SHAPES = {"kda_decode_b64_bounded_gate": dict(lb_gate=True, sigmoid_out=True)}
+                   "kda_decode_b64_bounded_gate": ("kda_decode_b64", "decode"),
+                   # the prefill at the same size with the per-channel decay, 32 qk heads
+                   "kda_prefill_b4_t4096": ("gdn_prefill_b4_t4096", "prefill")}
+EXTRA_SHAPES = {"kda_decode_b64_bounded_gate": dict(lb_gate=True, sigmoid_out=True),
+                "kda_prefill_b4_t4096": dict(kda=True, H_qk=32)}
+PREFILL_WORKLOADS = ("gdn_prefill_b4_t4096", "kda_prefill_b4_t4096")
 
 
 def make_workload(name, device):
@@ -592,15 +614,21 @@ def run_ours(args):
     if rank == 0 and not args.no_workloads:
         extra = {}
         for name in ("kda_decode_b64", "kda_decode_b64_bounded_gate", "kda_verify_b32_t4",
-                     "kda_verify_b32_t4_outputs_only", "kda_commit_b32_t4", "gdn_prefill_b4_t4096"):
+                     "kda_verify_b32_t4_outputs_only", "kda_commit_b32_t4", "gdn_prefill_b4_t4096",
+                     "kda_prefill_b4_t4096"):
             if name == main.name:
                 continue
             w = make_workload(name, device)
-            k = args.aux_steps if name != "gdn_prefill_b4_t4096" else max(3, args.aux_steps // 10)
+            k = args.aux_steps if name not in PREFILL_WORKLOADS else max(3, args.aux_steps // 10)
             wms = time_steps(w.step, 3, k, flush) / k
             r = roofline(w, wms, peaks)
             entry = {"value": round(w.units_per_step / (wms * 1e-3), 1), "unit": UNIT,
                      "ms_per_step": round(wms, 5), "kernel": w.kernel, "roofline": r}
+            if getattr(w, "alu_flops_per_launch", 0):
+                tf = w.alu_flops_per_launch / (wms * 1e-3) / 1e12
+                entry["alu"] = {"achieved": round(tf, 2), "peak": round(FP32_PEAK_TFLOPS, 1),
+                                "unit": "TFLOP/s", "frac": round(tf / FP32_PEAK_TFLOPS, 4),
+                                "peak_from": "152 SMs x 128 fp32 lanes x 2 x 2.07 GHz"}
             if getattr(w, "flops_per_launch", 0):
                 tf = w.flops_per_launch / (wms * 1e-3) / 1e12
                 entry["tensor"] = {"achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
@@ -626,7 +654,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(list(synth.WORKLOADS) + list(EXTRA_WORKLOADS)))
     ap.add_argument("--aux-steps", type=int, default=100)
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-workloads", action="store_true")

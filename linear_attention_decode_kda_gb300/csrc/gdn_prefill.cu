@@ -580,15 +580,24 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
     if (!ok && lane == 0) atomicOr(&g_prefill_error, 1u);
 }
 
-bool chunked_eligible(const gdn_shape_t &s, const StepArgs &a)
+// Shapes the tensor-core kernel takes (its pointer rules aside).
+bool chunked_shape(const gdn_shape_t &s)
 {
     const int group = s.H_v / s.H_qk;
+    const size_t C = 2 * static_cast<size_t>(s.H_qk) * s.d_k + static_cast<size_t>(s.H_v) * s.d_v;
     return s.gate_mode == GDN_GATE_PER_HEAD && s.d_k == PD && s.d_v == PD &&
            s.in_dtype == GDN_BF16 && (s.chunk == CH || s.chunk == 64) && group <= 8 &&
-           (reinterpret_cast<uintptr_t>(a.qkv) & 15u) == 0 &&
-           (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0 && (static_cast<size_t>(a.C) * 2) % 16 == 0 &&
-           static_cast<long long>(a.B) * a.T < (1LL << 31);
+           (C * 2) % 16 == 0 && static_cast<long long>(s.B) * s.T < (1LL << 31);
 }
+
+bool chunked_eligible(const gdn_shape_t &s, const StepArgs &a)
+{
+    return chunked_shape(s) && (reinterpret_cast<uintptr_t>(a.qkv) & 15u) == 0 &&
+           (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0;
+}
+
+// Shapes that run the two-kernel chunked form over a workspace.
+bool two_stage_shape(const gdn_shape_t &s) { return !chunked_shape(s) && kda_chunk_shape(s); }
 
 cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
 {
@@ -640,13 +649,15 @@ cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
 
 }  // namespace
 
-size_t prefill_workspace_bytes(const gdn_shape_t &) { return 0; }
+size_t prefill_workspace_bytes(const gdn_shape_t &s)
+{
+    return two_stage_shape(s) ? kda_chunk_workspace_bytes(s) : 0;
+}
 
 const char *prefill_variant(const gdn_shape_t &s, int num_sms)
 {
-    if (s.gate_mode == GDN_GATE_PER_HEAD && s.d_k == PD && s.d_v == PD && s.in_dtype == GDN_BF16 &&
-        (s.chunk == CH || s.chunk == 64) && s.H_v / s.H_qk <= 8)
-        return "chunked<128,32>";
+    if (chunked_shape(s)) return "chunked<128,32>";
+    if (two_stage_shape(s)) return "kda_chunked<16>";
     StepPlan plan;
     const int sms = num_sms > 0 ? num_sms : 148;
     const bool planned = s.T <= 4 ? plan_step(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, sms, &plan)
@@ -654,11 +665,15 @@ const char *prefill_variant(const gdn_shape_t &s, int num_sms)
     return planned ? plan.name : nullptr;
 }
 
-gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *, int num_sms,
+gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspace, int num_sms,
                          cudaStream_t stream)
 {
     if (chunked_eligible(s, a)) {
         cudaError_t e = launch_chunked(a, stream);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+    if (two_stage_shape(s)) {
+        cudaError_t e = launch_kda_chunked(a, workspace, stream);
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
     // the recurrent kernel over all T tokens: short runs take the step plan, long ones the

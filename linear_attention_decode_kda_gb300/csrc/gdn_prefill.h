@@ -22,4 +22,12 @@ gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspac
 // Reads and clears the chunked prefill kernel's device error word (synchronous).
 unsigned int take_prefill_error();
 
+// Two-kernel chunked form (gdn_kda_prefill.cu): d = 128, any gate, T > 4.
+bool kda_chunk_shape(const gdn_shape_t &s);
+size_t kda_chunk_workspace_bytes(const gdn_shape_t &s);
+// Queues the intra-chunk kernel, then the state kernel; `workspace` holds
+// kda_chunk_workspace_bytes(s) bytes, 16-byte aligned.
+cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t stream);
+unsigned int take_kda_prefill_error();
+
 }  // namespace gdn

@@ -142,8 +142,34 @@ def test_gate_variants_are_accepted(lib):
     s.gate_mode = gdn.GDN_GATE_LOWER_BOUND
     s.flags = gdn.GDN_FLAG_SIGMOID_GATE | gdn.GDN_FLAG_PDL
     assert gdn.gdn_kernel_variant(s, gdn.OP_DECODE) == "stream<128>"
-    s.T = 64  # the bounded per-channel gate has no chunked form: the recurrent kernel runs
-    assert not gdn.gdn_kernel_variant(s, gdn.OP_PREFILL).startswith("chunked")
+    s.T = 64  # the bounded per-channel gate takes the two-kernel chunked form
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "kda_chunked<16>"
+
+
+def test_prefill_routing_and_workspace(lib):
+    """Per-head decay, bf16 rows, d = 128: the tensor-core kernel, no workspace.
+    Per-channel decay (or fp32 rows, or another chunk) at d = 128 and T > 4: the
+    two-kernel form, one 37,376-byte block per (sequence, head, 16-token chunk).
+    Otherwise the recurrent kernel, no workspace."""
+    s = _shape(T=100, kda=False)
+    s.chunk = 64
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "chunked<128,32>"
+    assert gdn.gdn_prefill_workspace_bytes(s) == 0
+    s = _shape(T=100)
+    s.chunk = 64
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "kda_chunked<16>"
+    assert gdn.gdn_prefill_workspace_bytes(s) == 2 * 4 * 7 * 37376
+    s.in_dtype = gdn.GDN_F32
+    s.gate_mode = gdn.GDN_GATE_PER_HEAD
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "kda_chunked<16>"
+    s = _shape(T=4)
+    s.chunk = 64
+    assert gdn.gdn_prefill_workspace_bytes(s) == 0
+    assert not gdn.gdn_kernel_variant(s, gdn.OP_PREFILL).startswith(("chunked", "kda_chunked"))
+    s = _shape(T=100, d_k=64, d_v=64)
+    s.chunk = 64
+    assert gdn.gdn_prefill_workspace_bytes(s) == 0
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL).startswith("step<64")
 
 
 def test_variant_choice(lib):
