@@ -169,10 +169,14 @@ GDN_API gdn_status_t gdn_commit_accepted(const gdn_shape_t *shape, const gdn_ten
 /*
  * Chunked prefill of T >= 1 tokens per sequence: the same result as T decode
  * steps, computed in the chunked WY/UT form ("llama.cpp PR #84", chunked
- * KDA prefill) with chunk length shape->chunk.  conv_state and state are
- * advanced in place; out receives y for every token.  workspace must hold
- * gdn_prefill_workspace_bytes(shape) bytes (may be 0 bytes; then NULL is
- * accepted).
+ * KDA prefill).  conv_state and state are advanced in place; out receives y
+ * for every token.  Per-head decay with bf16 rows at d = 128 runs the
+ * tensor-core kernel in 32-token chunks (shape->chunk 32 or 64); the other
+ * d = 128 shapes with T > 4 run the two-kernel form in 16-token chunks
+ * (whatever shape->chunk asks, which must be > 0); the rest run the
+ * recurrent kernel.  workspace must hold gdn_prefill_workspace_bytes(shape)
+ * bytes, 16-byte aligned (may be 0 bytes; then NULL is accepted); the call
+ * owns it until the work queued on `stream` completes.
  */
 GDN_API gdn_status_t gdn_prefill_chunked(const gdn_shape_t *shape, const gdn_tensors_t *t,
                                  void *workspace, size_t workspace_bytes,
