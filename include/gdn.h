@@ -185,6 +185,33 @@ GDN_API gdn_status_t gdn_prefill_chunked(const gdn_shape_t *shape, const gdn_ten
 /* Bytes of device workspace gdn_prefill_chunked needs for this shape (0 on a bad shape). */
 GDN_API size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
 
+/* Bytes of the scratch gdn_prefill_chunked_static uses in place of a workspace. */
+#define GDN_PREFILL_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * gdn_prefill_chunked with no workspace argument, for callers that cannot
+ * allocate device memory around the call: a C host with no device allocator
+ * of its own, or a serving loop in which a cudaMalloc (which synchronises the
+ * device) would stall the work queued on its other streams.
+ *
+ * The scratch is one static device array of GDN_PREFILL_STATIC_SCRATCH_BYTES
+ * per device, reserved when the library's module loads; its address is looked
+ * up once per device.  The call allocates and frees nothing.  A shape whose
+ * gdn_prefill_workspace_bytes exceeds the scratch returns GDN_ERR_WORKSPACE
+ * before anything is queued (one sequence of 32 heads fits about 440 tokens).
+ * Nothing in the scratch has to start at zero: the first kernel writes every
+ * word the second one uses.
+ *
+ * Every call on a device shares that one scratch.  Two calls whose work
+ * overlaps in time (on different streams, or from different host threads
+ * without ordering) race on it and produce wrong results; calls queued on one
+ * stream run in order and are safe.  Arguments, results and the other errors
+ * are those of gdn_prefill_chunked.  The pages describe no such entry point;
+ * it is a deployment convenience around the same kernels.
+ */
+GDN_API gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *shape, const gdn_tensors_t *t,
+                                        gdn_stream_t stream);
+
 /*
  * Reads and clears the library's device error word on the current device.
  * Kernels that wait on an mbarrier give up after about two seconds instead of

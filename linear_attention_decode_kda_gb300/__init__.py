@@ -55,8 +55,11 @@ class GdnError(RuntimeError):
 
 
 EXPORTS = ("gdn_decode_step", "gdn_verify_T", "gdn_commit_accepted", "gdn_prefill_chunked",
-           "gdn_prefill_workspace_bytes", "gdn_device_status", "gdn_status_string",
-           "gdn_kernel_variant")
+           "gdn_prefill_workspace_bytes", "gdn_prefill_chunked_static", "gdn_device_status",
+           "gdn_status_string", "gdn_kernel_variant")
+
+# bytes of the library's own scratch behind gdn_prefill_chunked_static
+PREFILL_STATIC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 
@@ -84,6 +87,8 @@ def load():
     lib.gdn_commit_accepted.argtypes = [S, Tn, P, P]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked.argtypes = [S, Tn, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_chunked_static.restype = ctypes.c_int
+    lib.gdn_prefill_chunked_static.argtypes = [S, Tn, P]
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_prefill_workspace_bytes.argtypes = [S]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -128,6 +133,13 @@ def gdn_prefill_chunked(shape: GdnShape, tensors: GdnTensors, workspace: int = 0
     _check(load().gdn_prefill_chunked(ctypes.byref(shape), ctypes.byref(tensors),
                                       ctypes.c_void_p(workspace), workspace_bytes,
                                       ctypes.c_void_p(stream)), "gdn_prefill_chunked")
+
+
+def gdn_prefill_chunked_static(shape: GdnShape, tensors: GdnTensors, stream: int = 0) -> None:
+    """gdn_prefill_chunked on the library's static scratch: allocates nothing; calls
+    whose work overlaps in time race on the one scratch."""
+    _check(load().gdn_prefill_chunked_static(ctypes.byref(shape), ctypes.byref(tensors),
+                                             ctypes.c_void_p(stream)), "gdn_prefill_chunked_static")
 
 
 def gdn_prefill_workspace_bytes(shape: GdnShape) -> int:

@@ -110,6 +110,24 @@ bool plan_for(const gdn_shape_t *s, gdn::StepPlan *plan)
     return gdn::plan_step(s->d_k, s->B, s->H_v, s->H_v / s->H_qk, sms > 0 ? sms : 148, plan);
 }
 
+// Scratch of gdn_prefill_chunked_static, for callers that cannot allocate:
+// a module-scope device array, reserved when the module loads.  Its device
+// address is looked up once per device; writers race benignly (same value).
+static __device__ __align__(256) unsigned char g_prefill_scratch[GDN_PREFILL_STATIC_SCRATCH_BYTES];
+void *g_scratch_addr[kMaxDevices];
+
+void *static_scratch()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = p;
+    }
+    return g_scratch_addr[dev];
+}
+
 gdn_status_t run_step(const gdn_shape_t *s, const gdn::StepArgs &a, cudaStream_t stream)
 {
     gdn::StepPlan plan;
@@ -202,6 +220,31 @@ gdn_status_t gdn_prefill_chunked(const gdn_shape_t *s, const gdn_tensors_t *t, v
     const int sms = num_sms_current();
     return gdn::run_prefill(*s, a, workspace, sms > 0 ? sms : 148,
                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *s, const gdn_tensors_t *t,
+                                        gdn_stream_t stream)
+{
+    gdn_status_t rc = check_shape(s);
+    if (rc != GDN_OK) return rc;
+    if (s->T < 1) return GDN_ERR_SHAPE;
+    rc = check_tensors(s, t);
+    if (rc != GDN_OK) return rc;
+    if (s->chunk <= 0) return GDN_ERR_SHAPE;
+    const size_t need = gdn::prefill_workspace_bytes(*s);
+    if (need > GDN_PREFILL_STATIC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+    if (s->B == 0) return GDN_OK;
+    void *ws = nullptr;
+    if (need > 0) {
+        ws = static_scratch();
+        if (!ws) return GDN_ERR_CUDA;
+    }
+    // no clearing: the intra-chunk kernel writes every scratch word the state kernel uses
+    gdn::StepArgs a = step_args(s, t);
+    a.state_out = t->state;
+    a.conv_out = t->conv_state;
+    const int sms = num_sms_current();
+    return gdn::run_prefill(*s, a, ws, sms > 0 ? sms : 148, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *gdn_status_string(gdn_status_t status)
