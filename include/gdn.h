@@ -198,7 +198,7 @@ GDN_API size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
  * per device, reserved when the library's module loads; its address is looked
  * up once per device.  The call allocates and frees nothing.  A shape whose
  * gdn_prefill_workspace_bytes exceeds the scratch returns GDN_ERR_WORKSPACE
- * before anything is queued (one sequence of 32 heads fits about 440 tokens).
+ * before anything is queued (one sequence of 32 heads fits 480 tokens).
  * Nothing in the scratch has to start at zero: the first kernel writes every
  * word the second one uses.
  *

@@ -1,5 +1,6 @@
 // Chunked prefill for the per-channel decay (KDA), and for per-head decay shapes
-// the tensor-core kernel does not take: two kernels over a device workspace.
+// the single-kernel tensor-core prefill does not take: two kernels over a
+// device workspace.
 //
 // The form is the chunked WY/UT recurrence with one log-decay per key channel,
 // split the way "llama.cpp PR #84" splits its chunked KDA prefill (an intra-chunk
@@ -15,16 +16,17 @@
 // scaled.)  The per-token form it restates is the step of "Thirty tiny kernels
 // per layer"; T of these steps and this form agree up to rounding.
 //
-// kda_intra_kernel: one CTA per (sequence, head, chunk), all chunks at once.  It
-// runs the conv, the norms, the gates, the pair sums L and A and the forward
-// substitution, and writes W, U, e^G * Q, e^{G_last - G} * K, A and e^{G_last}
-// to the workspace (fp32).
-// kda_state_kernel: one CTA per (sequence, head).  The fp32 state lives in
-// registers; each chunk's block arrives by one TMA bulk copy into a ring of
-// three stages; the products run as packed fp32 FMAs; the gated RMSNorm and the
-// output store close each chunk.  The products are 16 x 128 x 128 per chunk: too
-// thin for the tensor-core pipe's M = 64/128 tiles without a transposed state
-// operand in shared memory, and fp32 keeps the state exact to rounding.
+// kda_intra_kernel: one CTA per (sequence, head, chunk), all chunks at once,
+// on the CUDA cores (the pair sums need an exponential per element).  It runs
+// the conv, the norms, the gates, L and A and the forward substitution, and
+// writes one block per chunk: the tensor-core operands W, e^G * Q,
+// (e^{G_last - G} * K)^T and A as fp16 hi/lo pairs, U and e^{G_last} in fp32.
+// kda_state_kernel: one CTA per (sequence, head) carries S through the chunks
+// on tcgen05.  S^T (lane = state column) is the fp32 accumulator in TMEM, with
+// a split-fp16 copy in shared memory as the A operand; per chunk
+//   P^T = S^T W^T                      -> V_new = U - P on the CUDA cores
+//   O^T = S^T (e^G Q)^T + V_new^T A^T,  S^T = e^{G_last} S^T + V_new^T (e^{G_last-G} K)
+// then the gated RMSNorm and the output store.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -33,6 +35,8 @@
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 #include "gdn_prefill.h"
+#include "gdn_tc.cuh"
+#include "gdn_tmap.h"
 
 namespace gdn {
 namespace {
@@ -41,24 +45,18 @@ using namespace dev;
 
 constexpr int KD = 128;  // d_k = d_v
 constexpr int KC = 16;   // tokens per chunk
-// Workspace block of one (sequence, head, chunk), in floats.  The three panels
-// the state kernel reads by row quarters keep 4 spare floats after every 32
-// channels, so the quarters of a row start in different shared-memory banks.
-constexpr int KP = 144;
-constexpr int OFF_W = 0;
-constexpr int OFF_Q = KC * KP;
-constexpr int OFF_K = 2 * KC * KP;
-constexpr int OFF_U = 3 * KC * KP;
-constexpr int OFF_A = OFF_U + KC * KD;
-constexpr int OFF_G = OFF_A + KC * KC;
-constexpr int BLOCK = OFF_G + KD;
-constexpr uint32_t BLOCK_BYTES = BLOCK * 4;
+// Workspace block of one (sequence, head, chunk), in bytes.  Tensor-core
+// operands are fp16 hi/lo pairs in the canonical K-major layout (tc::op_offset).
+constexpr int BW_WQ = 0;     // [W; e^G Q] [32 rows][128 i] (W rows 0-15): hi (8 KiB), then lo
+constexpr int BW_K = 16384;  // (e^{G_last - G} K)^T [128 i][16 t]: hi, lo
+constexpr int BW_M = 24576;  // A [16 t][16 s]: hi (512 B), then lo
+constexpr int BW_U = 25600;  // U [16 t][128 j], fp32
+constexpr int BW_G = 33792;  // e^{G_last} [128], fp32
+constexpr uint32_t BLOCK_BYTES = 34304;
+static_assert(BW_G + KD * 4 == BLOCK_BYTES, "block layout");
 static_assert(BLOCK_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 __device__ unsigned int g_kda_error;
-
-// position of channel r in a padded panel row
-__host__ __device__ constexpr int pidx(int r) { return r + ((r >> 5) << 2); }
 
 // Intra kernel staging rows: 136 floats, 4 spare after channel 63, so the two
 // channel halves of a row sit in different banks.
@@ -86,12 +84,14 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-__global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, float *ws)
+__global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned char *ws)
 {
-    __shared__ __align__(16) float qs[KC][SP];
-    __shared__ __align__(16) float ks[KC][SP];
-    __shared__ __align__(16) float vs[KC][SP];
-    __shared__ __align__(16) float gs[KC][SP];
+    // staging rows of q, k, v and G; they take the block image at the end
+    __shared__ __align__(128) float stg[4][KC][SP];
+    float(*qs)[SP] = stg[0];
+    float(*ks)[SP] = stg[1];
+    float(*vs)[SP] = stg[2];
+    float(*gs)[SP] = stg[3];
     __shared__ __align__(16) float Ls[KC][KC];
     __shared__ __align__(16) float As[KC][KC];
     __shared__ float bs[KC];
@@ -248,12 +248,12 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, float *ws
     }
     __syncthreads();
 
-    // ---- 3. (I + L) X = B by forward substitution, one column a thread:
-    // W's columns from beta e^G k, U's from beta v; then the state stage's operands
-    float *blk = ws + ((static_cast<size_t>(b) * a.H_v + h) * gridDim.x + n) * BLOCK;
+    // ---- 3. (I + L) X = B by forward substitution, one column a thread: W's
+    // columns from beta e^G k (threads 0-127), U's from beta v (128-255); then the
+    // block image in shared memory over the staging rows, copied out coalesced
+    float x[KC], y[KC], gl = 0.f;
     {
         const bool wside = tid < KD;
-        float x[KC];
 #pragma unroll
         for (int t = 0; t < KC; ++t)
             x[t] = bs[t] * (wside ? ks[t][hp(i)] * __expf(gs[t][hp(i)]) : vs[t][hp(i)]);
@@ -263,327 +263,291 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, float *ws
             for (int s = 0; s < t; ++s) x[t] = fmaf(-Ls[t][s], x[s], x[t]);
         if (wside) {
 #pragma unroll
-            for (int t = 0; t < KC; ++t) {
-                blk[OFF_W + t * KP + pidx(i)] = x[t];
-                blk[OFF_Q + t * KP + pidx(i)] = qs[t][hp(i)] * __expf(gs[t][hp(i)]);
-            }
+            for (int t = 0; t < KC; ++t) y[t] = qs[t][hp(i)] * __expf(gs[t][hp(i)]);
         } else {
             const float Gl = gs[KC - 1][hp(i)];
 #pragma unroll
-            for (int t = 0; t < KC; ++t) {
-                blk[OFF_U + t * KD + i] = x[t];
-                blk[OFF_K + t * KP + pidx(i)] = ks[t][hp(i)] * __expf(Gl - gs[t][hp(i)]);
-            }
-            blk[OFF_G + i] = __expf(Gl);
+            for (int t = 0; t < KC; ++t) y[t] = ks[t][hp(i)] * __expf(Gl - gs[t][hp(i)]);
+            gl = __expf(Gl);
         }
-        blk[OFF_A + tid] = As[tid >> 4][tid & 15];
     }
+    const float m = As[tid >> 4][tid & 15];
+    __syncthreads();  // the staging rows are read: they take the block image
+    unsigned char *img = reinterpret_cast<unsigned char *>(&stg[0][0][0]);
+    if (tid < KD) {
+#pragma unroll
+        for (int t = 0; t < KC; ++t) {
+            tc::put_split(img + BW_WQ, img + BW_WQ + 8192, tc::op_offset(t, i, KD), x[t]);
+            tc::put_split(img + BW_WQ, img + BW_WQ + 8192, tc::op_offset(KC + t, i, KD), y[t]);
+        }
+    } else {
+        float *U = reinterpret_cast<float *>(img + BW_U);
+#pragma unroll
+        for (int t = 0; t < KC; ++t) U[t * KD + i] = x[t];
+        tc::put_row8(img + BW_K, img + BW_K + 4096, tc::op_offset(i, 0, KC), y);
+        tc::put_row8(img + BW_K, img + BW_K + 4096, tc::op_offset(i, 8, KC), y + 8);
+        reinterpret_cast<float *>(img + BW_G)[i] = gl;
+    }
+    tc::put_split(img + BW_M, img + BW_M + 512, tc::op_offset(tid >> 4, tid & 15, KC), m);
+    __syncthreads();
+    uint4 *dst = reinterpret_cast<uint4 *>(
+        ws + ((static_cast<size_t>(b) * a.H_v + h) * gridDim.x + n) * BLOCK_BYTES);
+    const uint4 *src = reinterpret_cast<const uint4 *>(img);
+    for (int e = tid; e < static_cast<int>(BLOCK_BYTES / 16); e += 256) dst[e] = src[e];
 }
 
 // ---------------------------------------------------------------- state stage
 
 constexpr int NSTG = 3;
+// A stage holds the chunk's block, then its 16 output-gate rows (z, in dtype).
+constexpr int STAGE_Z = 34816;             // block bytes rounded up to 1 KiB
+constexpr int STAGE = STAGE_Z + KC * KD * 4;
+static_assert(STAGE_Z >= static_cast<int>(BLOCK_BYTES) && STAGE % 1024 == 0, "stage size");
+// TMEM columns
+constexpr int TM_S = 0;     // 128: S^T (lane j = state column j, column i = state row i)
+constexpr int TM_P = 128;   // 16: P^T = (W S)^T
+constexpr int TM_O = 144;   // 16: (e^G Q S)^T, then O^T
+constexpr uint32_t TM_COLS = 256;
+// dynamic shared memory (bytes)
+constexpr int SS_ST = NSTG * STAGE;             // split S^T [128 j][128 i]: hi (32 KiB), lo
+constexpr int SS_VN = SS_ST + 2 * KD * KD * 2;  // split V_new^T [128 j][16 t]: hi (4 KiB), lo
+constexpr int SS_SQ = SS_VN + 2 * KD * KC * 2;  // o^2 [16 t][SQS]
+constexpr int SQS = KD + 4;
+constexpr int SS_BYTES = SS_SQ + KC * SQS * 4;
 
-struct StateSmem {
-    float blk[NSTG][BLOCK];
-    float red[2][8][KC];  // per warp, per token: partial sums of o^2, by chunk parity
+struct StateShared {
+    float rinv[KC];
     uint64_t full[NSTG];
+    uint64_t mma_bar;
+    uint32_t tmem;
 };
 
-__device__ __forceinline__ float2 lo2(const float4 v) { return make_float2(v.x, v.y); }
-__device__ __forceinline__ float2 hi2(const float4 v) { return make_float2(v.z, v.w); }
-
-__device__ __forceinline__ void store_out2(void *out, size_t idx, int bf16, float a, float b)
+// Makes this thread's shared-memory writes visible to the tensor core, then syncs the CTA.
+__device__ __forceinline__ void publish_smem()
 {
-    if (bf16) {
-        *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + idx) =
-            __floats2bfloat162_rn(a, b);
-    } else {
-        *reinterpret_cast<float2 *>(reinterpret_cast<float *>(out) + idx) = make_float2(a, b);
-    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
 }
 
-// Thread layout: lane = row quarter rq (rows 32 rq .. 32 rq + 31) + 4 x column
-// pair; warp w holds column pairs 8w .. 8w + 7, so a quad of lanes covers two
-// full columns and the sums over rows are two shuffles.
-__global__ void __launch_bounds__(256, 1) kda_state_kernel(StepArgs a, const float *ws, int nchunk)
+// Thread layout: ch = tid % 128 is the state column j (TMEM lane j, warp w
+// reaching lanes 32 (w % 4) ..); half = tid / 128 splits the row-wise work.
+__global__ void __launch_bounds__(256, 1)
+kda_state_kernel(StepArgs a, const unsigned char *ws, int nchunk, const __grid_constant__ CUtensorMap tmz)
 {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    StateSmem &sm = *reinterpret_cast<StateSmem *>(smem_raw);
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ __align__(16) StateShared ps;
     const int h = blockIdx.x, b = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rq = lane & 3;
-    const int c0 = 2 * (warp * 8 + (lane >> 2));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int ch = tid & (KD - 1), half = tid >> 7;
+    const int lb = 32 * (warp & 3);
     const size_t head = static_cast<size_t>(b) * a.H_v + h;
-    const float *blocks = ws + head * nchunk * BLOCK;
+    const unsigned char *blocks = ws + head * nchunk * static_cast<size_t>(BLOCK_BYTES);
+    unsigned char *st_hi = sm + SS_ST, *st_lo = sm + SS_ST + KD * KD * 2;
+    unsigned char *vn_hi = sm + SS_VN, *vn_lo = sm + SS_VN + KD * KC * 2;
+    float *sq = reinterpret_cast<float *>(sm + SS_SQ);
 
+    if (warp == 0) tc::tmem_alloc(&ps.tmem, TM_COLS);
     if (tid == 0) {
-        for (int s = 0; s < NSTG; ++s) mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < NSTG; ++s) mbar_init(&ps.full[s], 1);
+        mbar_init(&ps.mma_bar, 1);
         fence_mbar_init();
     }
+    tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < NSTG && s < nchunk; ++s) {
-            mbar_expect_tx(&sm.full[s], BLOCK_BYTES);
-            tma_load_1d(sm.blk[s], blocks + static_cast<size_t>(s) * BLOCK, BLOCK_BYTES, &sm.full[s]);
-        }
+    tc::fence_after_sync();
+    const uint32_t tm = ps.tmem;
+    const uint32_t zbytes = KC * KD * (a.in_bf16 ? 2u : 4u);
+    auto issue = [&](int n) {
+        const int s = n % NSTG;
+        mbar_expect_tx(&ps.full[s], BLOCK_BYTES + zbytes);
+        tma_load_1d(sm + s * STAGE, blocks + static_cast<size_t>(n) * BLOCK_BYTES, BLOCK_BYTES, &ps.full[s]);
+        // rows past the last token of the batch read as zero; rows of the next sequence are unused
+        tma_load_3d(sm + s * STAGE + STAGE_Z, &tmz, 0, h, b * a.T + n * KC, &ps.full[s]);
+    };
+    // thread 128 (warp 4) issues every copy and every product
+    constexpr int ISSUER = 128;
+    if (tid == ISSUER) {
+        prefetch_tensormap(&tmz);
+        for (int n = 0; n < NSTG && n < nchunk; ++n) issue(n);
     }
 
-    // state rows 32 rq + 2p, +1 of columns c0 (sc0) and c0 + 1 (sc1), as row pairs
-    float2 sc0[16], sc1[16];
+    // state S[i][j] -> TMEM S^T and its split operand; half 0 takes rows i < 64
     {
-        const float *S = a.state_in + head * KD * KD + c0;
+        const float *Sg = a.state_in + head * KD * KD;
+        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+            float v[16];
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-            const int r = 32 * rq + 2 * p;
-            const float2 x = *reinterpret_cast<const float2 *>(S + static_cast<size_t>(r) * KD);
-            const float2 y = *reinterpret_cast<const float2 *>(S + static_cast<size_t>(r + 1) * KD);
-            sc0[p] = make_float2(x.x, y.x);
-            sc1[p] = make_float2(x.y, y.y);
+            for (int ii = 0; ii < 16; ++ii) v[ii] = Sg[(i0 + ii) * KD + ch];
+            tc::tmem_st16(tc::taddr(tm, lb, TM_S + i0), v);
+            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0, KD), v);
+            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, KD), v + 8);
         }
     }
-    const float nw0 = a.norm_w[c0], nw1 = a.norm_w[c0 + 1];
+    publish_smem();
+
+    const float nw = a.norm_w[ch];
     bool ok = true;
+    uint32_t mma_ph = 0;
+    auto mma_wait = [&]() {
+        if (ok) ok = mbar_wait_bounded(&ps.mma_bar, mma_ph);
+        mma_ph ^= 1u;
+        tc::fence_after_sync();
+    };
+    const uint32_t id16 = tc::idesc_f16(128, KC, false), id32 = tc::idesc_f16(128, 2 * KC, false),
+                   id128 = tc::idesc_f16(128, KD, false);
+    // 1. [P | Q']^T = S^T [W; e^G Q]^T of chunk n (one N = 32 product), issued once its
+    // block is in and S^T's operand is current
+    auto issue_p = [&](int n) {
+        const unsigned char *Bn = sm + (n % NSTG) * STAGE;
+        if (ok) ok = mbar_wait_bounded(&ps.full[n % NSTG], static_cast<uint32_t>((n / NSTG) & 1));
+        tc::fence_after_sync();
+        tc::mma_split(tm + TM_P, tc::smem_u32(st_hi), tc::smem_u32(st_lo), tc::smem_u32(Bn + BW_WQ),
+                      tc::smem_u32(Bn + BW_WQ + 8192), KD, id32, false);
+        tc::mma_commit(&ps.mma_bar);
+    };
+    if (tid == ISSUER) issue_p(0);
 
 #pragma unroll 1
     for (int n = 0; n < nchunk; ++n) {
-        const int st = n % NSTG;
         const int t0 = n * KC, nt = min(KC, a.T - t0);
-        // output-gate inputs of this lane's tokens 4 rq .. 4 rq + 3, issued early
-        float z0[4], z1[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = 4 * rq + j;
-            z0[j] = z1[j] = 0.f;
-            if (t < nt) {
-                const size_t idx = ((static_cast<size_t>(b) * a.T + t0 + t) * a.H_v + h) * KD + c0;
-                z0[j] = ld_in(a.z, idx, a.in_bf16);
-                z1[j] = ld_in(a.z, idx + 1, a.in_bf16);
-            }
-        }
-        if (!mbar_wait_bounded(&sm.full[st], static_cast<uint32_t>((n / NSTG) & 1))) ok = false;
-        const float *B = sm.blk[st];
+        const unsigned char *B = sm + (n % NSTG) * STAGE;
+        if (ok) ok = mbar_wait_bounded(&ps.full[n % NSTG], static_cast<uint32_t>((n / NSTG) & 1));
+        mma_wait();  // P^T of this chunk
 
-        // 1. P = W S0 and Q' = (e^G Q) S0.  Tokens go in groups {j, j+4, j+8, j+12}
-        // (16 independent accumulator chains), each group summed over the quad at
-        // once so that lane rq keeps token j + 4 rq.  pv[0..3][j]: P col c0,
-        // P col c0+1, Q' col c0, Q' col c0+1 of token 4 rq + j
-        float pv[4][4];
+        // 2. V_new = U - P as the split operand V_new^T; S^T <- e^{G_last} S^T by state row
+        if (half == 0) {
+            float p[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_P), p);
+            const float *U = reinterpret_cast<const float *>(B + BW_U);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float2 acc[4][4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[g][c] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float4 w4[4], q4[4];
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int t = j + 4 * g;
-                    w4[g] = *reinterpret_cast<const float4 *>(B + OFF_W + t * KP + 36 * rq + 4 * m);
-                    q4[g] = *reinterpret_cast<const float4 *>(B + OFF_Q + t * KP + 36 * rq + 4 * m);
-                }
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    acc[g][0] = __ffma2_rn(lo2(w4[g]), sc0[2 * m], acc[g][0]);
-                    acc[g][1] = __ffma2_rn(lo2(w4[g]), sc1[2 * m], acc[g][1]);
-                    acc[g][2] = __ffma2_rn(lo2(q4[g]), sc0[2 * m], acc[g][2]);
-                    acc[g][3] = __ffma2_rn(lo2(q4[g]), sc1[2 * m], acc[g][3]);
-                }
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    acc[g][0] = __ffma2_rn(hi2(w4[g]), sc0[2 * m + 1], acc[g][0]);
-                    acc[g][1] = __ffma2_rn(hi2(w4[g]), sc1[2 * m + 1], acc[g][1]);
-                    acc[g][2] = __ffma2_rn(hi2(q4[g]), sc0[2 * m + 1], acc[g][2]);
-                    acc[g][3] = __ffma2_rn(hi2(q4[g]), sc1[2 * m + 1], acc[g][3]);
-                }
-            }
-            float r[4][4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) r[g][c] = acc[g][c].x + acc[g][c].y;
-            // xor 2: lanes with rq & 2 keep tokens g = 2, 3, the others g = 0, 1
-            const bool up2 = (rq & 2) != 0;
-#pragma unroll
-            for (int g = 0; g < 2; ++g)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float send = up2 ? r[g][c] : r[g + 2][c];
-                    const float keep = up2 ? r[g + 2][c] : r[g][c];
-                    r[g][c] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-                }
-            // xor 1: lanes with rq & 1 keep the odd one: g = rq
-            const bool up1 = (rq & 1) != 0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float send = up1 ? r[0][c] : r[1][c];
-                const float keep = up1 ? r[1][c] : r[0][c];
-                pv[c][j] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-            }
+            for (int t = 0; t < KC; ++t) p[t] = U[t * KD + ch] - p[t];
+            tc::put_row8(vn_hi, vn_lo, tc::op_offset(ch, 0, KC), p);
+            tc::put_row8(vn_hi, vn_lo, tc::op_offset(ch, 8, KC), p + 8);
         }
-
-        // 2. V_new = U - P for this lane's tokens, then gathered for all 16
-        float V0[KC], V1[KC];
         {
-            float vn0[4], vn1[4];
+            const float *gl = reinterpret_cast<const float *>(B + BW_G);
+            for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+                float sv[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 u = *reinterpret_cast<const float2 *>(B + OFF_U + (4 * rq + j) * KD + c0);
-                vn0[j] = u.x - pv[0][j];
-                vn1[j] = u.y - pv[1][j];
-            }
-            float a0[8], a1[8];
-            const bool up1 = (rq & 1) != 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float r0 = __shfl_xor_sync(0xffffffffu, vn0[j], 1);
-                const float r1 = __shfl_xor_sync(0xffffffffu, vn1[j], 1);
-                a0[j] = up1 ? r0 : vn0[j];
-                a0[j + 4] = up1 ? vn0[j] : r0;
-                a1[j] = up1 ? r1 : vn1[j];
-                a1[j + 4] = up1 ? vn1[j] : r1;
-            }
-            const bool up2 = (rq & 2) != 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float r0 = __shfl_xor_sync(0xffffffffu, a0[j], 2);
-                const float r1 = __shfl_xor_sync(0xffffffffu, a1[j], 2);
-                V0[j] = up2 ? r0 : a0[j];
-                V0[j + 8] = up2 ? a0[j] : r0;
-                V1[j] = up2 ? r1 : a1[j];
-                V1[j + 8] = up2 ? a1[j] : r1;
+                for (int ii = 0; ii < 16; ++ii) sv[ii] *= gl[i0 + ii];
+                tc::tmem_st16(tc::taddr(tm, lb, TM_S + i0), sv);
             }
         }
+        publish_smem();
 
-        // 3. O = Q' + A V_new (A is zero above the diagonal)
-        float o0[4], o1[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 *ar = reinterpret_cast<const float4 *>(B + OFF_A + (4 * rq + j) * KC);
-            float x0 = pv[2][j], x1 = pv[3][j];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float4 av = ar[m];
-                x0 = fmaf(av.x, V0[4 * m], x0);
-                x1 = fmaf(av.x, V1[4 * m], x1);
-                x0 = fmaf(av.y, V0[4 * m + 1], x0);
-                x1 = fmaf(av.y, V1[4 * m + 1], x1);
-                x0 = fmaf(av.z, V0[4 * m + 2], x0);
-                x1 = fmaf(av.z, V1[4 * m + 2], x1);
-                x0 = fmaf(av.w, V0[4 * m + 3], x0);
-                x1 = fmaf(av.w, V1[4 * m + 3], x1);
-            }
-            o0[j] = x0;
-            o1[j] = x1;
+        // 3. O^T = Q'^T + V_new^T A^T;  S^T += V_new^T (e^{G_last - G} K)
+        if (tid == ISSUER) {
+            tc::fence_after_sync();
+            const uint32_t vh = tc::smem_u32(vn_hi), vl = tc::smem_u32(vn_lo);
+            tc::mma_split(tm + TM_O, vh, vl, tc::smem_u32(B + BW_M), tc::smem_u32(B + BW_M + 512), KC,
+                          id16, true);
+            tc::mma_split(tm + TM_S, vh, vl, tc::smem_u32(B + BW_K), tc::smem_u32(B + BW_K + 4096), KC,
+                          id128, true);
+            tc::mma_commit(&ps.mma_bar);
         }
+        mma_wait();
 
-        // 4. S = Diag(e^{G_last}) S0 + Kd^T V_new
+        // 4. each half: o, its squares and the output gate of tokens 8 half .. +7, and
+        // the new S^T of rows 64 half .. +63 as the next chunk's operand
+        float o[8], gz[8];
+        tc::tmem_ld8(tc::taddr(tm, lb, TM_O + 8 * half), o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = 8 * half + j;
+            sq[t * SQS + ch] = o[j] * o[j];
+            const float zz = a.in_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(B + STAGE_Z)[t * KD + ch])
+                                       : reinterpret_cast<const float *>(B + STAGE_Z)[t * KD + ch];
+            gz[j] = nw * (a.sig_gate ? fast_sigmoid(zz) : fast_silu(zz));
+        }
+        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+            float sv[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
+            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0, KD), sv);
+            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, KD), sv + 8);
+        }
+        publish_smem();  // the stage is consumed; o^2 and the S^T operand are in
+
+        // 5. gated RMSNorm over the 128 columns of each token (16 threads a token)
         {
-            const float4 *gl = reinterpret_cast<const float4 *>(B + OFF_G + 32 * rq);
+            const int t = tid >> 4, part = tid & 15;
+            float s_ = 0.f;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const float4 g4 = gl[m];
-                sc0[2 * m] = __fmul2_rn(sc0[2 * m], lo2(g4));
-                sc0[2 * m + 1] = __fmul2_rn(sc0[2 * m + 1], hi2(g4));
-                sc1[2 * m] = __fmul2_rn(sc1[2 * m], lo2(g4));
-                sc1[2 * m + 1] = __fmul2_rn(sc1[2 * m + 1], hi2(g4));
-            }
-#pragma unroll
-            for (int t = 0; t < KC; ++t) {
-                const float4 *kr = reinterpret_cast<const float4 *>(B + OFF_K + t * KP + 36 * rq);
-                const float2 v0 = make_float2(V0[t], V0[t]), v1 = make_float2(V1[t], V1[t]);
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const float4 k4 = kr[m];
-                    sc0[2 * m] = __ffma2_rn(lo2(k4), v0, sc0[2 * m]);
-                    sc0[2 * m + 1] = __ffma2_rn(hi2(k4), v0, sc0[2 * m + 1]);
-                    sc1[2 * m] = __ffma2_rn(lo2(k4), v1, sc1[2 * m]);
-                    sc1[2 * m + 1] = __ffma2_rn(hi2(k4), v1, sc1[2 * m + 1]);
-                }
-            }
+            for (int j = 0; j < 8; ++j) s_ += sq[t * SQS + 8 * part + j];
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 1);
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 2);
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 4);
+            s_ += __shfl_xor_sync(0xffffffffu, s_, 8);
+            if (part == 0) ps.rinv[t] = 1.0f / sqrtf(s_ / static_cast<float>(KD) + a.eps_norm);
         }
-
-        // 5. gated RMSNorm over the head's 128 columns
-        float ss[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) ss[j] = fmaf(o0[j], o0[j], o1[j] * o1[j]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], off);
-        float(*rd)[KC] = sm.red[n & 1];
-        if ((lane >> 2) == 0)
-            *reinterpret_cast<float4 *>(&rd[warp][4 * rq]) = make_float4(ss[0], ss[1], ss[2], ss[3]);
-        __syncthreads();  // the stage is consumed and the partial sums are in
-        if (tid == 0 && n + NSTG < nchunk) {
-            mbar_expect_tx(&sm.full[st], BLOCK_BYTES);
-            tma_load_1d(sm.blk[st], blocks + static_cast<size_t>(n + NSTG) * BLOCK, BLOCK_BYTES,
-                        &sm.full[st]);
+        __syncthreads();
+        if (tid == ISSUER) {
+            if (n + NSTG < nchunk) issue(n + NSTG);
+            if (n + 1 < nchunk) issue_p(n + 1);  // overlaps this chunk's output rows
         }
-        float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float4 r4 = *reinterpret_cast<const float4 *>(&rd[w][4 * rq]);
-            tot.x += r4.x;
-            tot.y += r4.y;
-            tot.z += r4.z;
-            tot.w += r4.w;
-        }
-        const float tv[4] = {tot.x, tot.y, tot.z, tot.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = 4 * rq + j;
+        for (int j = 0; j < 8; ++j) {
+            const int t = 8 * half + j;
             if (t < nt) {
-                const float rinv = 1.0f / sqrtf(tv[j] / static_cast<float>(KD) + a.eps_norm);
-                const float g0 = a.sig_gate ? sigmoid_f(z0[j]) : silu_f(z0[j]);
-                const float g1 = a.sig_gate ? sigmoid_f(z1[j]) : silu_f(z1[j]);
-                const size_t idx = ((static_cast<size_t>(b) * a.T + t0 + t) * a.H_v + h) * KD + c0;
-                store_out2(a.out, idx, a.out_bf16, o0[j] * rinv * nw0 * g0, o1[j] * rinv * nw1 * g1);
+                const size_t idx = ((static_cast<size_t>(b) * a.T + t0 + t) * a.H_v + h) * KD + ch;
+                const float yv = o[j] * ps.rinv[t] * gz[j];
+                if (a.out_bf16)
+                    reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(yv);
+                else
+                    reinterpret_cast<float *>(a.out)[idx] = yv;
             }
         }
     }
-    if (!ok) atomicOr(&g_kda_error, 1u);
 
-    // final state
+    // final state S[i][j] from S^T (lane j)
     {
-        float *So = a.state_out + head * KD * KD + c0;
+        float *So = a.state_out + head * KD * KD;
+        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+            float sv[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-            const int r = 32 * rq + 2 * p;
-            *reinterpret_cast<float2 *>(So + static_cast<size_t>(r) * KD) = make_float2(sc0[p].x, sc1[p].x);
-            *reinterpret_cast<float2 *>(So + static_cast<size_t>(r + 1) * KD) =
-                make_float2(sc0[p].y, sc1[p].y);
+            for (int ii = 0; ii < 16; ++ii) So[(i0 + ii) * KD + ch] = sv[ii];
         }
     }
     // final conv window: rows T, T+1, T+2 of [kept window; the T new rows].  v
     // channels by their head, q and k channels by the group's first value head
     {
-        const int i = tid & (KD - 1);
         const int hq = h / a.group;
         const size_t C = static_cast<size_t>(a.C);
-        int ch[2], nc = 0;
-        if (tid < KD) {
-            ch[nc++] = 2 * a.H_qk * KD + h * KD + i;
+        int chn[2], nc = 0;
+        if (half == 0) {
+            chn[nc++] = 2 * a.H_qk * KD + h * KD + ch;
         } else if (h % a.group == 0) {
-            ch[nc++] = hq * KD + i;
-            ch[nc++] = a.H_qk * KD + hq * KD + i;
+            chn[nc++] = hq * KD + ch;
+            chn[nc++] = a.H_qk * KD + hq * KD + ch;
         }
         for (int m = 0; m < nc; ++m) {
-            const int c = ch[m];
-            float x[3];
+            const int c = chn[m];
+            float x3[3];
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
                 const int idx = a.T + j;
-                x[j] = idx < 3 ? a.conv_in[(static_cast<size_t>(b) * 3 + idx) * C + c]
-                               : ld_in(a.qkv, (static_cast<size_t>(b) * a.T + idx - 3) * C + c, a.in_bf16);
+                x3[j] = idx < 3 ? a.conv_in[(static_cast<size_t>(b) * 3 + idx) * C + c]
+                                : ld_in(a.qkv, (static_cast<size_t>(b) * a.T + idx - 3) * C + c, a.in_bf16);
             }
 #pragma unroll
-            for (int j = 0; j < 3; ++j) a.conv_out[(static_cast<size_t>(b) * 3 + j) * C + c] = x[j];
+            for (int j = 0; j < 3; ++j) a.conv_out[(static_cast<size_t>(b) * 3 + j) * C + c] = x3[j];
         }
     }
+    if (!ok && tid == ISSUER) {
+        // a wait gave up: let the copies and products still in flight land
+        // (bounded) before the shared memory and TMEM are released
+        for (int s = 0; s < NSTG && s < nchunk; ++s) {
+            const int last = s + NSTG * ((nchunk - 1 - s) / NSTG);
+            mbar_wait_bounded(&ps.full[s], static_cast<uint32_t>((last / NSTG) & 1));
+        }
+        mbar_wait_bounded(&ps.mma_bar, mma_ph ^ 1u);
+        atomicOr(&g_kda_error, 1u);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
 }
 
 }  // namespace
@@ -592,6 +556,11 @@ bool kda_chunk_shape(const gdn_shape_t &s)
 {
     return s.d_k == KD && s.d_v == KD && s.T > 4 && s.conv_K == 4 &&
            static_cast<long long>(s.B) * s.T < (1LL << 31);
+}
+
+bool kda_chunk_pointers_ok(const StepArgs &a)
+{
+    return (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0;  // the output-gate rows go by TMA
 }
 
 size_t kda_chunk_workspace_bytes(const gdn_shape_t &s)
@@ -607,18 +576,28 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    constexpr int SMEM = static_cast<int>(sizeof(StateSmem));
+    constexpr int SMEM = SS_BYTES;
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(kda_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     const int nchunk = (a.T + KC - 1) / KC;
-    float *ws = static_cast<float *>(workspace);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    CUtensorMap tmz;
+    {   // z as [B*T][H_v][128] in the input dtype, boxes of 16 tokens x 1 head x 128 channels
+        const uint64_t es = a.in_bf16 ? 2 : 4;
+        const uint64_t dim[3] = {KD, static_cast<uint64_t>(a.H_v), static_cast<uint64_t>(a.B) * a.T};
+        const uint64_t stride[2] = {KD * es, static_cast<uint64_t>(a.H_v) * KD * es};
+        const uint32_t box[3] = {KD, 1, KC};
+        if (!encode_tiled(&tmz, a.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                          a.z, dim, stride, box))
+            return cudaErrorInvalidValue;
+    }
     kda_intra_kernel<<<dim3(nchunk, a.H_v, a.B), 256, 0, stream>>>(a, ws);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kda_state_kernel<<<dim3(a.H_v, a.B), 256, SMEM, stream>>>(a, ws, nchunk);
+    kda_state_kernel<<<dim3(a.H_v, a.B), 256, SMEM, stream>>>(a, ws, nchunk, tmz);
     return cudaGetLastError();
 }
 

@@ -81,12 +81,10 @@ __device__ __forceinline__ void put_h(unsigned char *base, uint32_t off, float v
 {
     *reinterpret_cast<__half *>(base + off) = __float2half_rn(v);
 }
-__device__ __forceinline__ void put_split(unsigned char *hi, unsigned char *lo, uint32_t off, float v)
-{
-    const __half h = __float2half_rn(v);
-    *reinterpret_cast<__half *>(hi + off) = h;
-    *reinterpret_cast<__half *>(lo + off) = __float2half_rn(v - __half2float(h));
-}
+using tc::mma_chain;
+using tc::mma_split;
+using tc::put_row8;
+using tc::put_split;
 __device__ __forceinline__ float get_h(const unsigned char *base, uint32_t off)
 {
     return __half2float(*reinterpret_cast<const __half *>(base + off));
@@ -94,21 +92,6 @@ __device__ __forceinline__ float get_h(const unsigned char *base, uint32_t off)
 __device__ __forceinline__ float get_bf16(const unsigned char *base, uint32_t off)
 {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
-}
-
-// 8 consecutive K values of one row of a K-major operand (offset 16-byte aligned),
-// as one 128-bit store per half of the split (or of the plain fp16 operand).
-__device__ __forceinline__ void put_row8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *v)
-{
-    __half2 h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half a = __float2half_rn(v[2 * i]), b = __float2half_rn(v[2 * i + 1]);
-        h[i] = __halves2half2(a, b);
-        l[i] = __floats2half2_rn(v[2 * i] - __half2float(a), v[2 * i + 1] - __half2float(b));
-    }
-    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<const uint4 *>(h);
-    if (lo) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<const uint4 *>(l);
 }
 
 // SiLU with the hardware exponential and fast division (relative error ~1e-6,
@@ -130,23 +113,6 @@ __device__ __forceinline__ void publish_smem()
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
-}
-
-// D (+)= A B^T over K in steps of 16 (single thread).
-__device__ __forceinline__ void mma_chain(uint32_t d, uint32_t a, uint32_t b, int kdim,
-                                          uint32_t idesc, bool acc)
-{
-    for (int k0 = 0; k0 < kdim; k0 += 16)
-        tc::mma_f16(d, tc::op_desc(a, k0, kdim), tc::op_desc(b, k0, kdim), idesc, acc || k0 > 0);
-}
-
-// D (+)= (A_hi + A_lo)(B_hi + B_lo)^T without the lo*lo term.
-__device__ __forceinline__ void mma_split(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh,
-                                          uint32_t bl, int kdim, uint32_t idesc, bool acc)
-{
-    mma_chain(d, ah, bh, kdim, idesc, acc);
-    mma_chain(d, ah, bl, kdim, idesc, true);
-    mma_chain(d, al, bh, kdim, idesc, true);
 }
 
 __global__ void __launch_bounds__(PT, 1)
@@ -672,7 +638,7 @@ gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspac
         cudaError_t e = launch_chunked(a, stream);
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
-    if (two_stage_shape(s)) {
+    if (two_stage_shape(s) && kda_chunk_pointers_ok(a)) {
         cudaError_t e = launch_kda_chunked(a, workspace, stream);
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }

@@ -24,6 +24,8 @@ unsigned int take_prefill_error();
 
 // Two-kernel chunked form (gdn_kda_prefill.cu): d = 128, any gate, T > 4.
 bool kda_chunk_shape(const gdn_shape_t &s);
+// The kernels' pointer rule beyond the ABI's: z 16-byte aligned (else the recurrent kernel runs).
+bool kda_chunk_pointers_ok(const StepArgs &a);
 size_t kda_chunk_workspace_bytes(const gdn_shape_t &s);
 // Queues the intra-chunk kernel, then the state kernel; `workspace` holds
 // kda_chunk_workspace_bytes(s) bytes, 16-byte aligned.

@@ -13,6 +13,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdn {
@@ -115,6 +116,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 8 consecutive fp32 columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
 {
     asm volatile(
@@ -128,6 +142,47 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
         "r"(__float_as_uint(v[15]))
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Tensor-core operands are fp16 (11 significant bits); precision-critical ones
+// are kept as hi + lo pairs (x ~ hi + lo) and multiplied as hi*hi + hi*lo + lo*hi.
+__device__ __forceinline__ void put_split(unsigned char *hi, unsigned char *lo, uint32_t off, float v)
+{
+    const __half h = __float2half_rn(v);
+    *reinterpret_cast<__half *>(hi + off) = h;
+    *reinterpret_cast<__half *>(lo + off) = __float2half_rn(v - __half2float(h));
+}
+
+// 8 consecutive K values of one row of a K-major operand (offset 16-byte aligned),
+// as one 128-bit store per half of the split (lo may be null: a plain fp16 operand).
+__device__ __forceinline__ void put_row8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *v)
+{
+    __half2 h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half a = __float2half_rn(v[2 * i]), b = __float2half_rn(v[2 * i + 1]);
+        h[i] = __halves2half2(a, b);
+        l[i] = __floats2half2_rn(v[2 * i] - __half2float(a), v[2 * i + 1] - __half2float(b));
+    }
+    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<const uint4 *>(h);
+    if (lo) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<const uint4 *>(l);
+}
+
+// D (+)= A B^T over K in steps of 16 (single thread).
+__device__ __forceinline__ void mma_chain(uint32_t d, uint32_t a, uint32_t b, int kdim,
+                                          uint32_t idesc, bool acc)
+{
+    for (int k0 = 0; k0 < kdim; k0 += 16)
+        mma_f16(d, op_desc(a, k0, kdim), op_desc(b, k0, kdim), idesc, acc || k0 > 0);
+}
+
+// D (+)= (A_hi + A_lo)(B_hi + B_lo)^T without the lo*lo term.
+__device__ __forceinline__ void mma_split(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh,
+                                          uint32_t bl, int kdim, uint32_t idesc, bool acc)
+{
+    mma_chain(d, ah, bh, kdim, idesc, acc);
+    mma_chain(d, ah, bl, kdim, idesc, true);
+    mma_chain(d, al, bh, kdim, idesc, true);
 }
 
 // TMEM address of (lane, column) for the warp's lane quadrant.

@@ -149,7 +149,7 @@ def test_gate_variants_are_accepted(lib):
 def test_prefill_routing_and_workspace(lib):
     """Per-head decay, bf16 rows, d = 128: the tensor-core kernel, no workspace.
     Per-channel decay (or fp32 rows, or another chunk) at d = 128 and T > 4: the
-    two-kernel form, one 37,376-byte block per (sequence, head, 16-token chunk).
+    two-kernel form, one 34,304-byte block per (sequence, head, 16-token chunk).
     Otherwise the recurrent kernel, no workspace."""
     s = _shape(T=100, kda=False)
     s.chunk = 64
@@ -158,7 +158,7 @@ def test_prefill_routing_and_workspace(lib):
     s = _shape(T=100)
     s.chunk = 64
     assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "kda_chunked<16>"
-    assert gdn.gdn_prefill_workspace_bytes(s) == 2 * 4 * 7 * 37376
+    assert gdn.gdn_prefill_workspace_bytes(s) == 2 * 4 * 7 * 34304
     s.in_dtype = gdn.GDN_F32
     s.gate_mode = gdn.GDN_GATE_PER_HEAD
     assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "kda_chunked<16>"

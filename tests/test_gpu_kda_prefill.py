@@ -2,8 +2,9 @@
 ("llama.cpp PR #84", chunked KDA prefill: an intra-chunk stage over all chunks,
 then a state stage over the chunks), against T sequential oracle steps.
 
-The kernels compute in fp32 throughout, so they are held to the decode bar
-(1e-3), tighter than the tensor-core prefill's 1e-2."""
+The intra-chunk kernel computes in fp32 and the state kernel's tcgen05 products
+take split-fp16 operands (hi + lo, about 22 significant bits), so the path is held
+to the decode bar (1e-3), tighter than the tensor-core prefill's 1e-2."""
 
 import dataclasses
 
@@ -95,6 +96,28 @@ def test_per_head_gate_on_the_two_kernel_form(bf16_in, chunk):
     shape = synth.Shape(B=2, T=77, H_qk=2, H_v=4, d_k=128, d_v=128, kda=False,
                         bf16_in=bf16_in, chunk=chunk)
     _check(shape, seed=45, slow=True)
+
+
+def test_misaligned_output_gate_rows_take_the_recurrent_kernel():
+    """The state kernel brings z in by TMA (16-byte aligned base); a z that is only
+    element-aligned runs on the recurrent kernel instead, with the same results."""
+    shape = synth.Shape(B=2, T=40, H_qk=2, H_v=2, d_k=128, d_v=128, kda=True, chunk=64)
+    params, inp, state = _case(shape, 47, True)
+    case = dev.upload(shape, params, inp, state)
+    buf = torch.empty(case.z.numel() + 8, dtype=case.z.dtype, device="cuda")
+    zv = buf[1:1 + case.z.numel()].view(case.z.shape)
+    zv.copy_(case.z)
+    case.z = zv
+    assert zv.data_ptr() % 16 != 0
+    sh = case.abi_shape()
+    n = gdn.gdn_prefill_workspace_bytes(sh)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    gdn.gdn_prefill_chunked(sh, case.abi_tensors(), ws.data_ptr(), n, stream())
+    torch.cuda.synchronize()
+    gdn.gdn_device_status()
+    ref = oracle_run(shape, params, inp, state)
+    assert_close(case.out.reshape(ref["y"].shape), ref["y"], DECODE_TOL, "y")
+    assert_close(case.state, ref["state"], DECODE_TOL, "state")
 
 
 def test_kda_prefill_resumes_across_calls_and_matches_one_call():

@@ -35,10 +35,10 @@ def test_scratch_limit_is_checked_before_anything_is_queued():
     assert gdn.gdn_prefill_workspace_bytes(s) > gdn.PREFILL_STATIC_SCRATCH_BYTES
     rc = lib.gdn_prefill_chunked_static(ctypes.byref(s), ctypes.byref(_fake_tensors()), None)
     assert rc == gdn.GDN_ERR_WORKSPACE
-    # 448 tokens of one 32-head sequence (28 chunks of 16) are the most that fit
-    s = _shape(B=1, T=448, H_qk=32, H_v=32)
+    # 480 tokens of one 32-head sequence (30 chunks of 16) are the most that fit
+    s = _shape(B=1, T=480, H_qk=32, H_v=32)
     assert gdn.gdn_prefill_workspace_bytes(s) <= gdn.PREFILL_STATIC_SCRATCH_BYTES
-    s.T = 449
+    s.T = 481
     assert gdn.gdn_prefill_workspace_bytes(s) > gdn.PREFILL_STATIC_SCRATCH_BYTES
     # the ordinary argument checks come first, as in gdn_prefill_chunked
     assert lib.gdn_prefill_chunked_static(None, ctypes.byref(_fake_tensors()), None) == \
