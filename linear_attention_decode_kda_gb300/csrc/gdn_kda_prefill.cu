@@ -68,6 +68,26 @@ __device__ __forceinline__ int hp(int i) { return i + ((i >> 6) << 2); }
 __device__ __forceinline__ float fast_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float fast_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
+// 2^x and log2(x) on the hardware approximations (relative error about 2^-22).
+// The intra kernel keeps the cumulative log-decays in log2 units, so every decay
+// factor it forms is one ex2 of a difference <= 0.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float2 lo2(const float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(const float4 v) { return make_float2(v.z, v.w); }
+
 // After the call lane l holds the warp-wide sum of v[l].
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
 {
@@ -84,6 +104,7 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned char *ws)
 {
     // staging rows of q, k, v and G; they take the block image at the end
@@ -105,18 +126,24 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
     const int hq = h / a.group;
     const size_t C = static_cast<size_t>(a.C);
     const size_t row0 = static_cast<size_t>(b) * a.T + t0;
+    auto ld = [&](const void *p, size_t idx) {
+        return BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[idx])
+                    : reinterpret_cast<const float *>(p)[idx];
+    };
 
     // channel c's rows t0 - 3 .. t0 + 15: the three before t0 come from the
-    // sequence, or from the kept window before its start; padded tokens read 0
+    // sequence, or from the kept window before its start; rows past the
+    // sequence repeat its last row (their outputs are zeroed)
     auto load_rows = [&](int c, float(&x)[KC + 3]) {
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             const int tau = t0 - 3 + j;
-            x[j] = tau >= 0 ? ld_in(a.qkv, (static_cast<size_t>(b) * a.T + tau) * C + c, a.in_bf16)
+            x[j] = tau >= 0 ? ld(a.qkv, (static_cast<size_t>(b) * a.T + tau) * C + c)
                             : a.conv_in[(static_cast<size_t>(b) * 3 + (3 + tau)) * C + c];
         }
+        const size_t base = static_cast<size_t>(b) * a.T;
 #pragma unroll
-        for (int t = 0; t < KC; ++t) x[3 + t] = t < nt ? ld_in(a.qkv, (row0 + t) * C + c, a.in_bf16) : 0.f;
+        for (int t = 0; t < KC; ++t) x[3 + t] = ld(a.qkv, (base + min(t0 + t, a.T - 1)) * C + c);
     };
     // 4-tap causal conv + SiLU of those rows
     auto conv_rows = [&](int c, const float(&x)[KC + 3], float(&y)[KC]) {
@@ -132,7 +159,7 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
     };
 
     // ---- 1. conv, squares for the L2 norms, gates; padded tokens are zero
-    if (tid < KC) bs[tid] = tid < nt ? fast_sigmoid(ld_in(a.beta, (row0 + tid) * a.H_v + h, a.in_bf16)) : 0.f;
+    if (tid < KC) bs[tid] = tid < nt ? fast_sigmoid(ld(a.beta, (row0 + tid) * a.H_v + h)) : 0.f;
     Ls[tid >> 4][tid & 15] = 0.f;
     As[tid >> 4][tid & 15] = 0.f;
     float q[KC], k[KC];
@@ -158,22 +185,26 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         load_rows(cv, xv);
 #pragma unroll
         for (int t = 0; t < KC; ++t) {
-            const size_t bth = (row0 + t) * a.H_v + h;
-            fl[t] = t < nt ? (a.kda ? ld_in(a.f, bth * KD + i, a.in_bf16) : ld_in(a.f, bth, a.in_bf16)) : 0.f;
+            const size_t bth = (static_cast<size_t>(b) * a.T + min(t0 + t, a.T - 1)) * a.H_v + h;
+            fl[t] = a.kda ? ld(a.f, bth * KD + i) : ld(a.f, bth);
         }
         float v[KC];
         conv_rows(cv, xv, v);
 #pragma unroll
         for (int t = 0; t < KC; ++t) vs[t][hp(i)] = v[t];
-        // log-decays of channel i summed along the chunk.  Softplus gates:
-        // g = -exp(A_log) softplus(f + dt_bias); lower-bound gate: g = lb sigmoid(-a f)
+        // log-decays of channel i summed along the chunk, in log2 units.  Softplus
+        // gates: g = -exp(A_log) softplus(f + dt_bias), with softplus(x) = max(x, 0)
+        // + ln(1 + e^-|x|); lower-bound gate: g = lb sigmoid(-a f)
         const float A = a.lb_gate ? a.A_log[h] : expf(a.A_log[h]);
-        const float lbv = a.lb_gate ? a.dt_bias[h] : 0.f;
+        const float lbv = a.lb_gate ? a.dt_bias[h] * kLog2e : 0.f;
         const float dtb = a.lb_gate ? 0.f : (a.kda ? a.dt_bias[static_cast<size_t>(h) * KD + i] : a.dt_bias[h]);
         float G = 0.f;
 #pragma unroll
         for (int t = 0; t < KC; ++t) {
-            if (t < nt) G += a.lb_gate ? lbv * fast_sigmoid(-A * fl[t]) : -A * softplus_f(fl[t] + dtb);
+            const float x = fl[t] + dtb;
+            const float g2 = a.lb_gate ? lbv * fast_sigmoid(-A * fl[t])
+                                       : -A * fmaf(fmaxf(x, 0.f), kLog2e, lg2(1.0f + ex2(-fabsf(x) * kLog2e)));
+            if (t < nt) G += g2;
             gs[t][hp(i)] = G;
         }
     }
@@ -203,6 +234,9 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
             }
             s = p;
             const int base = 68 * (tid & 1);
+            // two channels at a time on the packed fp32 pipe
+            float2 kk2 = make_float2(0.f, 0.f), qk2 = kk2;
+            const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll 4
             for (int m = 0; m < 64; m += 4) {
                 const float4 g1 = *reinterpret_cast<const float4 *>(&gs[t][base + m]);
@@ -210,19 +244,15 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
                 const float4 k1 = *reinterpret_cast<const float4 *>(&ks[t][base + m]);
                 const float4 k0 = *reinterpret_cast<const float4 *>(&ks[s][base + m]);
                 const float4 q1 = *reinterpret_cast<const float4 *>(&qs[t][base + m]);
-                float e = __expf(g1.x - g0.x);
-                kk = fmaf(k1.x * k0.x, e, kk);
-                qk = fmaf(q1.x * k0.x, e, qk);
-                e = __expf(g1.y - g0.y);
-                kk = fmaf(k1.y * k0.y, e, kk);
-                qk = fmaf(q1.y * k0.y, e, qk);
-                e = __expf(g1.z - g0.z);
-                kk = fmaf(k1.z * k0.z, e, kk);
-                qk = fmaf(q1.z * k0.z, e, qk);
-                e = __expf(g1.w - g0.w);
-                kk = fmaf(k1.w * k0.w, e, kk);
-                qk = fmaf(q1.w * k0.w, e, qk);
+                const float2 dl = __ffma2_rn(lo2(g0), neg1, lo2(g1)), dh = __ffma2_rn(hi2(g0), neg1, hi2(g1));
+                const float2 el = make_float2(ex2(dl.x), ex2(dl.y)), eh = make_float2(ex2(dh.x), ex2(dh.y));
+                kk2 = __ffma2_rn(__fmul2_rn(lo2(k1), lo2(k0)), el, kk2);
+                qk2 = __ffma2_rn(__fmul2_rn(lo2(q1), lo2(k0)), el, qk2);
+                kk2 = __ffma2_rn(__fmul2_rn(hi2(k1), hi2(k0)), eh, kk2);
+                qk2 = __ffma2_rn(__fmul2_rn(hi2(q1), hi2(k0)), eh, qk2);
             }
+            kk = kk2.x + kk2.y;
+            qk = qk2.x + qk2.y;
         } else {
             t = tid - 240;
 #pragma unroll 4
@@ -256,19 +286,19 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         const bool wside = tid < KD;
 #pragma unroll
         for (int t = 0; t < KC; ++t)
-            x[t] = bs[t] * (wside ? ks[t][hp(i)] * __expf(gs[t][hp(i)]) : vs[t][hp(i)]);
+            x[t] = bs[t] * (wside ? ks[t][hp(i)] * ex2(gs[t][hp(i)]) : vs[t][hp(i)]);
 #pragma unroll
         for (int t = 1; t < KC; ++t)
 #pragma unroll
             for (int s = 0; s < t; ++s) x[t] = fmaf(-Ls[t][s], x[s], x[t]);
         if (wside) {
 #pragma unroll
-            for (int t = 0; t < KC; ++t) y[t] = qs[t][hp(i)] * __expf(gs[t][hp(i)]);
+            for (int t = 0; t < KC; ++t) y[t] = qs[t][hp(i)] * ex2(gs[t][hp(i)]);
         } else {
             const float Gl = gs[KC - 1][hp(i)];
 #pragma unroll
-            for (int t = 0; t < KC; ++t) y[t] = ks[t][hp(i)] * __expf(Gl - gs[t][hp(i)]);
-            gl = __expf(Gl);
+            for (int t = 0; t < KC; ++t) y[t] = ks[t][hp(i)] * ex2(Gl - gs[t][hp(i)]);
+            gl = ex2(Gl);
         }
     }
     const float m = As[tid >> 4][tid & 15];
@@ -594,7 +624,10 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
                           a.z, dim, stride, box))
             return cudaErrorInvalidValue;
     }
-    kda_intra_kernel<<<dim3(nchunk, a.H_v, a.B), 256, 0, stream>>>(a, ws);
+    if (a.in_bf16)
+        kda_intra_kernel<true><<<dim3(nchunk, a.H_v, a.B), 256, 0, stream>>>(a, ws);
+    else
+        kda_intra_kernel<false><<<dim3(nchunk, a.H_v, a.B), 256, 0, stream>>>(a, ws);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kda_state_kernel<<<dim3(a.H_v, a.B), 256, SMEM, stream>>>(a, ws, nchunk, tmz);
