@@ -326,6 +326,8 @@ class SingleLaunch(Workload):
         self.host_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         self.abi_shape = self.case.abi_shape()
         self.kernel = gdn.gdn_kernel_variant(self.abi_shape, op)
+        # kernels one call launches: the two-kernel chunked prefill launches two
+        self.kernels_per_launch = 2 if (self.kernel or "").startswith("kda_chunked") else 1
         # dense products of the chunked form at the chunk length the kernel runs
         m = re.match(r"chunked<\d+,(\d+)>", self.kernel or "") if op == gdn.OP_PREFILL else None
         self.flops_per_launch = (prefill_flops(dataclasses.replace(s, chunk=int(m.group(1))))
@@ -608,7 +610,7 @@ def run_ours(args):
             "e2e": {"value": round(whole_job_rate(main.units_per_step, args.steps, world,
                                                   ms_e2e), 2), "unit": UNIT,
                     "h2d_bytes_per_step": main.h2d_bytes, "d2h_bytes_per_step": main.d2h_bytes},
-            "gpu_launches": main.launches_per_step * args.steps,
+            "gpu_launches": main.launches_per_step * getattr(main, "kernels_per_launch", 1) * args.steps,
             "clocks": clk.summary()}
 
     if rank == 0 and not args.no_workloads:
