@@ -375,6 +375,70 @@ class SingleLaunch(Workload):
         self.host_out[j].copy_(self.out[j], non_blocking=True)
 
 
+class LayerDecode(Workload):
+    """One KDA layer per step, projections included (gdn_layer_decode): the layer
+    input x [B, d_model] bf16 -> q/k/v, f, beta, z rows -> the step -> x_out."""
+
+    D_MODEL, RANK = 4096, 128
+
+    def __init__(self, name, shape, device):
+        import torch
+
+        import linear_attention_decode_kda_gb300 as gdn
+        from synth import device as dev
+        self.gdn = gdn
+        self.name = name
+        s = dataclasses.replace(shape, bf16_in=False)  # fp32 rows between the launches
+        self.shape = s
+        D, R = self.D_MODEL, self.RANK
+        params = synth.make_params(s)
+        state = synth.make_state(s)
+        W = synth.make_layer_weights(s, D, R)
+        self.n = 4  # distinct inputs, cycled
+        xs = np.stack([synth.make_layer_input(s, D, step=i) for i in range(self.n)])
+        zero = synth.Inputs(np.zeros((s.B, 1, s.C), np.float32),
+                            np.zeros((s.B, 1, s.H_v, s.d_k), np.float32),
+                            np.zeros((s.B, 1, s.H_v), np.float32),
+                            np.zeros((s.B, 1, s.H_v, s.d_v), np.float32))
+        self.case = dev.upload(s, params, zero, state, device=device)
+        self.abi_shape = self.case.abi_shape()
+        self.w = {k: dev.to_torch(getattr(W, k), True, device) for k in W.FIELDS}
+        self.weights = gdn.layer_weights_from_torch(D, R, **self.w)
+        self.x = dev.to_torch(xs, True, device)
+        self.host_x = dev.to_torch(xs, True, None).pin_memory()
+        self.x_out = torch.empty((self.n, s.B, D), dtype=torch.float32, device=device)
+        self.host_out = torch.empty(self.x_out.shape, dtype=torch.float32).pin_memory()
+        self.ws_bytes = gdn.gdn_layer_workspace_bytes(self.abi_shape, self.weights)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
+        self.tensors = self.case.abi_tensors()
+        self.kernel = "proj + " + (gdn.gdn_kernel_variant(self.abi_shape, gdn.OP_DECODE) or "?")
+        self.launches_per_step = 1
+        self.kernels_per_launch = 4
+        self.units_per_step = s.B
+        wbytes = sum(int(v.numel()) * 2 for v in self.w.values())
+        self.weight_bytes = wbytes
+        self.bytes_per_launch = wbytes + s.B * D * (2 + 4) + algorithmic_bytes(s, "decode")
+        self.h2d_bytes = s.B * D * 2
+        self.d2h_bytes = s.B * D * 4
+
+    def _launch(self, j):
+        import torch
+        self.gdn.gdn_layer_decode(self.abi_shape, self.weights, self.x[j], self.x_out[j],
+                                  self.tensors, self.ws.data_ptr(), self.ws_bytes,
+                                  torch.cuda.current_stream().cuda_stream)
+
+    def step(self, i):
+        self._launch(i % self.n)
+
+    def e2e_step(self, i):
+        j = i % self.n
+        self.x[j].copy_(self.host_x[j], non_blocking=True)
+        self._launch(j)
+        self.host_out[j].copy_(self.x_out[j], non_blocking=True)
+
+
+LAYER_WORKLOADS = {"kda_layer_decode_b1": 1, "kda_layer_decode_b64": 64}
+
 # The verify workload's two calls of a speculative step without per-token states:
 # a verify that writes outputs only, then the in-place commit of the accepted tokens.
 EXTRA_WORKLOADS = {"kda_verify_b32_t4_outputs_only": ("kda_verify_b32_t4", "verify_outputs"),
@@ -390,6 +454,9 @@ PREFILL_WORKLOADS = ("gdn_prefill_b4_t4096", "kda_prefill_b4_t4096")
 
 def make_workload(name, device):
     import linear_attention_decode_kda_gb300 as gdn
+    if name in LAYER_WORKLOADS:
+        shape = dataclasses.replace(synth.WORKLOADS["kda_decode_b64"]["shape"], B=LAYER_WORKLOADS[name])
+        return LayerDecode(name, shape, device)
     spec = synth.WORKLOADS.get(name)
     if name == "kda_decode_b1_34layers":
         return DecodeLayers(name, spec, device)
@@ -617,7 +684,7 @@ def run_ours(args):
         extra = {}
         for name in ("kda_decode_b64", "kda_decode_b64_bounded_gate", "kda_verify_b32_t4",
                      "kda_verify_b32_t4_outputs_only", "kda_commit_b32_t4", "gdn_prefill_b4_t4096",
-                     "kda_prefill_b4_t4096"):
+                     "kda_prefill_b4_t4096", "kda_layer_decode_b1", "kda_layer_decode_b64"):
             if name == main.name:
                 continue
             w = make_workload(name, device)
@@ -657,7 +724,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(list(synth.WORKLOADS) + list(EXTRA_WORKLOADS)))
+                    choices=sorted(list(synth.WORKLOADS) + list(EXTRA_WORKLOADS) +
+                                   list(LAYER_WORKLOADS)))
     ap.add_argument("--aux-steps", type=int, default=100)
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-workloads", action="store_true")

@@ -213,6 +213,47 @@ GDN_API gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *shape, const 
                                         gdn_stream_t stream);
 
 /*
+ * Weights of one KDA layer's projections, all bf16, row-major, 16-byte
+ * aligned.  C = 2*H_qk*d_k + H_v*d_v as for qkv.
+ */
+typedef struct {
+    int32_t d_model;     /* width of the layer input x and output x_out (% 8 == 0)   */
+    int32_t rank;        /* width of the low-rank gate chains (% 8 == 0)             */
+    const void *w_qkv;   /* [C][d_model]: q of every qk head, k, then v rows          */
+    const void *w_fa;    /* [rank][d_model]: f_a                                      */
+    const void *w_fb;    /* [H_v*d_k][rank]: f_b, the per-channel gate logits         */
+    const void *w_ga;    /* [rank][d_model]: g_a                                      */
+    const void *w_gb;    /* [H_v*d_v][rank]: g_b, the output-gate rows z              */
+    const void *w_beta;  /* [H_v][d_model]: beta logits                               */
+    const void *w_o;     /* [d_model][H_v*d_v]: output projection                     */
+} gdn_layer_weights_t;
+
+/*
+ * One decode step of a whole KDA layer for B sequences (T = 1): the
+ * projections around the step fused into four launches.  From the layer input
+ * x ([B][d_model] bf16, 16-byte aligned):
+ *   qkv = x w_qkv^T, f_a = x w_fa^T, g_a = x w_ga^T, beta = x w_beta^T   (one launch)
+ *   f = f_a w_fb^T, z = g_a w_gb^T                                       (one launch)
+ *   the step of gdn_decode_step on those rows                            (the step)
+ *   x_out = y w_o^T                                                      (one launch)
+ * "Thirty tiny kernels per layer" (the decode budget: these projections are
+ * ~90% of a KDA layer's decode time, as weight streaming) and "llama.cpp PR
+ * #84" (f_a with g_a and beta, f_b with g_b, as single launches) describe the
+ * chain.  Activations stay fp32 between the launches: t->qkv, f, beta, z and out
+ * are caller scratch in the step's layouts with shape->in_dtype and
+ * shape->out_dtype GDN_F32, 16-byte aligned; conv_w, A_log, dt_bias, norm_w,
+ * conv_state and state are the step's.  gate_mode must be a per-channel gate.
+ * workspace holds gdn_layer_workspace_bytes bytes (the low-rank rows),
+ * 16-byte aligned.  x_out is [B][d_model] fp32.
+ */
+GDN_API gdn_status_t gdn_layer_decode(const gdn_shape_t *shape, const gdn_layer_weights_t *w,
+                              const void *x, float *x_out, const gdn_tensors_t *t,
+                              void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Bytes of workspace gdn_layer_decode needs (0 on bad arguments). */
+GDN_API size_t gdn_layer_workspace_bytes(const gdn_shape_t *shape, const gdn_layer_weights_t *w);
+
+/*
  * Reads and clears the library's device error word on the current device.
  * Kernels that wait on an mbarrier give up after about two seconds instead of
  * hanging and record the time-out there; their outputs are then invalid.

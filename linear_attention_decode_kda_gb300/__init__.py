@@ -55,11 +55,18 @@ class GdnError(RuntimeError):
 
 
 EXPORTS = ("gdn_decode_step", "gdn_verify_T", "gdn_commit_accepted", "gdn_prefill_chunked",
-           "gdn_prefill_workspace_bytes", "gdn_prefill_chunked_static", "gdn_device_status",
-           "gdn_status_string", "gdn_kernel_variant")
+           "gdn_prefill_workspace_bytes", "gdn_prefill_chunked_static", "gdn_layer_decode",
+           "gdn_layer_workspace_bytes", "gdn_device_status", "gdn_status_string",
+           "gdn_kernel_variant")
 
 # bytes of the library's own scratch behind gdn_prefill_chunked_static
 PREFILL_STATIC_SCRATCH_BYTES = 32 << 20
+
+class GdnLayerWeights(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("rank", ctypes.c_int32)] + \
+               [(n, ctypes.c_void_p) for n in
+                ("w_qkv", "w_fa", "w_fb", "w_ga", "w_gb", "w_beta", "w_o")]
+
 
 _lib = None
 
@@ -89,6 +96,11 @@ def load():
     lib.gdn_prefill_chunked.argtypes = [S, Tn, P, ctypes.c_size_t, P]
     lib.gdn_prefill_chunked_static.restype = ctypes.c_int
     lib.gdn_prefill_chunked_static.argtypes = [S, Tn, P]
+    W = ctypes.POINTER(GdnLayerWeights)
+    lib.gdn_layer_decode.restype = ctypes.c_int
+    lib.gdn_layer_decode.argtypes = [S, W, P, P, Tn, P, ctypes.c_size_t, P]
+    lib.gdn_layer_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_layer_workspace_bytes.argtypes = [S, W]
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_prefill_workspace_bytes.argtypes = [S]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -140,6 +152,26 @@ def gdn_prefill_chunked_static(shape: GdnShape, tensors: GdnTensors, stream: int
     whose work overlaps in time race on the one scratch."""
     _check(load().gdn_prefill_chunked_static(ctypes.byref(shape), ctypes.byref(tensors),
                                              ctypes.c_void_p(stream)), "gdn_prefill_chunked_static")
+
+
+def gdn_layer_decode(shape: GdnShape, weights: GdnLayerWeights, x, x_out, tensors: GdnTensors,
+                     workspace: int = 0, workspace_bytes: int = 0, stream: int = 0) -> None:
+    """x: [B, d_model] bf16, x_out: [B, d_model] fp32 (tensors or addresses)."""
+    _check(load().gdn_layer_decode(ctypes.byref(shape), ctypes.byref(weights),
+                                   ctypes.c_void_p(_ptr(x)), ctypes.c_void_p(_ptr(x_out)),
+                                   ctypes.byref(tensors), ctypes.c_void_p(workspace),
+                                   workspace_bytes, ctypes.c_void_p(stream)), "gdn_layer_decode")
+
+
+def gdn_layer_workspace_bytes(shape: GdnShape, weights: GdnLayerWeights) -> int:
+    return int(load().gdn_layer_workspace_bytes(ctypes.byref(shape), ctypes.byref(weights)))
+
+
+def layer_weights_from_torch(d_model: int, rank: int, **w) -> GdnLayerWeights:
+    """Weights as bf16 device tensors (keyword per field of GdnLayerWeights)."""
+    return GdnLayerWeights(d_model=d_model, rank=rank,
+                           **{k: _ptr(w[k]) for k in ("w_qkv", "w_fa", "w_fb", "w_ga", "w_gb",
+                                                      "w_beta", "w_o")})
 
 
 def gdn_prefill_workspace_bytes(shape: GdnShape) -> int:

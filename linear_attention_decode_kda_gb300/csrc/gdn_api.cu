@@ -247,6 +247,72 @@ gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *s, const gdn_tensors_
     return gdn::run_prefill(*s, a, ws, sms > 0 ? sms : 148, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t gdn_layer_workspace_bytes(const gdn_shape_t *s, const gdn_layer_weights_t *w)
+{
+    if (check_shape(s) != GDN_OK || !w || w->rank <= 0 || s->B < 0) return 0;
+    return static_cast<size_t>(s->B) * 2 * w->rank * sizeof(float);
+}
+
+gdn_status_t gdn_layer_decode(const gdn_shape_t *s, const gdn_layer_weights_t *w, const void *x,
+                              float *x_out, const gdn_tensors_t *t, void *workspace,
+                              size_t workspace_bytes, gdn_stream_t stream)
+{
+    gdn_status_t rc = check_shape(s);
+    if (rc != GDN_OK) return rc;
+    if (s->T != 1 || s->gate_mode == GDN_GATE_PER_HEAD || s->in_dtype != GDN_F32 ||
+        s->out_dtype != GDN_F32)
+        return GDN_ERR_SHAPE;
+    rc = check_tensors(s, t);
+    if (rc != GDN_OK) return rc;
+    if (!w || !x || !x_out || !w->w_qkv || !w->w_fa || !w->w_fb || !w->w_ga || !w->w_gb ||
+        !w->w_beta || !w->w_o)
+        return GDN_ERR_NULL;
+    if (w->d_model <= 0 || w->rank <= 0 || w->d_model % 8 || w->rank % 8) return GDN_ERR_SHAPE;
+    const void *wp[] = {w->w_qkv, w->w_fa, w->w_fb, w->w_ga, w->w_gb, w->w_beta, w->w_o, x,
+                        t->qkv, t->f, t->beta, t->z, t->out};
+    for (const void *p : wp)
+        if (!aligned16(p)) return GDN_ERR_ALIGN;
+    if (!aligned(x_out, 4)) return GDN_ERR_ALIGN;
+    const size_t need = gdn_layer_workspace_bytes(s, w);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return GDN_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return GDN_ERR_ALIGN;
+    gdn::StepPlan plan;
+    if (!plan_for(s, &plan)) return GDN_ERR_UNSUPPORTED;
+    if (s->B == 0) return GDN_OK;
+    const int B = s->B, D = w->d_model, R = w->rank, C = 2 * s->H_qk * s->d_k + s->H_v * s->d_v;
+    const int HK = s->H_v * s->d_k, HV = s->H_v * s->d_v;
+    float *lr = static_cast<float *>(workspace);  // [B][2R]: f_a, then g_a
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *qkv = static_cast<float *>(const_cast<void *>(t->qkv));
+    float *f = static_cast<float *>(const_cast<void *>(t->f));
+    float *beta = static_cast<float *>(const_cast<void *>(t->beta));
+    float *z = static_cast<float *>(const_cast<void *>(t->z));
+    const gdn::ProjSlotDesc in[4] = {
+        {w->w_qkv, x, qkv, C, D, D, C, 1},
+        {w->w_fa, x, lr, R, D, D, 2 * R, 1},
+        {w->w_ga, x, lr + R, R, D, D, 2 * R, 1},
+        {w->w_beta, x, beta, s->H_v, D, D, s->H_v, 1},
+    };
+    const gdn::ProjSlotDesc gate[2] = {
+        {w->w_fb, lr, f, HK, R, 2 * R, HK, 0},
+        {w->w_gb, lr + R, z, HV, R, 2 * R, HV, 0},
+    };
+    const gdn::ProjSlotDesc out[1] = {{w->w_o, t->out, x_out, D, HV, HV, D, 0}};
+    for (const auto &d : in)
+        if (!gdn::proj_slot_ok(d)) return GDN_ERR_ALIGN;
+    for (const auto &d : gate)
+        if (!gdn::proj_slot_ok(d)) return GDN_ERR_ALIGN;
+    if (!gdn::proj_slot_ok(out[0])) return GDN_ERR_ALIGN;
+    if (gdn::launch_proj(in, 4, B, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_proj(gate, 2, B, st) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn::StepArgs a = step_args(s, t);
+    a.state_out = t->state;
+    a.conv_out = t->conv_state;
+    rc = run_step(s, a, st);
+    if (rc != GDN_OK) return rc;
+    return gdn::launch_proj(out, 1, B, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 const char *gdn_status_string(gdn_status_t status)
 {
     switch (status) {

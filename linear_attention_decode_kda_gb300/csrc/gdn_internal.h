@@ -49,6 +49,20 @@ bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
 bool stream_eligible(const StepArgs &a);
 cudaError_t launch_stream(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
 
+// Weight-streaming projections around the step (gdn_proj.cu): per slot,
+// y[b][n] = sum_k x[b][k] w[n][k] with w bf16 [N][K] (row-major, 16-byte aligned,
+// K % 8 == 0), x fp32 or bf16 rows of stride ldx (16-byte aligned), y fp32 rows
+// of stride ldy.  One launch covers up to kMaxProjSlots slots.
+constexpr int kMaxProjSlots = 4;
+struct ProjSlotDesc {
+    const void *w;
+    const void *x;
+    float *y;
+    int N, K, ldx, ldy, x_bf16;
+};
+bool proj_slot_ok(const ProjSlotDesc &d);
+cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_t stream);
+
 // Read and clear the step kernels' device error words (synchronous).
 unsigned int take_stream_error();
 unsigned int take_step_error();

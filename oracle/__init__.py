@@ -146,6 +146,42 @@ def run_chunked(shape, params, inputs, conv_state, state, chunk: int, *, o_raw: 
     return out
 
 
+def project(x, w):
+    """A linear projection, y[b][n] = sum_k x[b][k] w[n][k], in fp64 (the layer's
+    q/k/v, gate, beta and output projections around the step, "Thirty tiny
+    kernels per layer", the KDA decode budget)."""
+    return np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
+
+
+def layer_decode(shape, params, weights, x, conv_state, state, nthreads: Optional[int] = None,
+                 lib=None):
+    """One decode token of a whole KDA layer: the projections (fp64), the step on
+    the projected rows, the output projection.  f = f_b(f_a(x)), z = g_b(g_a(x))
+    (the low-rank gate chains), qkv and beta straight from x.  The rows enter the
+    step as fp32, the width the step's C interface takes.  Returns dict(rows=...,
+    y, x_out, conv_state, state)."""
+    s = shape
+    assert s.T == 1 and s.kda
+    W = weights
+    qkv = project(x, W.w_qkv)
+    f = project(project(x, W.w_fa), W.w_fb)
+    z = project(project(x, W.w_ga), W.w_gb)
+    beta = project(x, W.w_beta)
+
+    class _Rows:
+        pass
+
+    rows = _Rows()
+    rows.qkv = qkv.reshape(s.B, 1, s.C)
+    rows.f = f.reshape(s.B, 1, s.H_v, s.d_k)
+    rows.beta = beta.reshape(s.B, 1, s.H_v)
+    rows.z = z.reshape(s.B, 1, s.H_v, s.d_v)
+    out = run(s, params, rows, conv_state, state, nthreads=nthreads, lib=lib)
+    out["x_out"] = project(out["y"].reshape(s.B, s.H_v * s.d_v), W.w_o)
+    out["rows"] = dict(qkv=qkv, f=f, beta=beta, z=z)
+    return out
+
+
 def conv(shape, qkv, conv_w, conv_state, lib=None):
     """a1 alone: returns (xhat [B,T,C], advanced conv_state)."""
     lib = lib or load()

@@ -251,5 +251,45 @@ def make_state(shape: Shape, seed: int = 0, layer: int = 0) -> State:
     return State(conv, S)
 
 
+@dataclasses.dataclass
+class LayerWeights:
+    """Projection weights of one KDA layer, bf16 values held in fp32 arrays."""
+    d_model: int
+    rank: int
+    w_qkv: np.ndarray   # [C, d_model]
+    w_fa: np.ndarray    # [rank, d_model]
+    w_fb: np.ndarray    # [H_v * d_k, rank]
+    w_ga: np.ndarray    # [rank, d_model]
+    w_gb: np.ndarray    # [H_v * d_v, rank]
+    w_beta: np.ndarray  # [H_v, d_model]
+    w_o: np.ndarray     # [d_model, H_v * d_v]
+
+    FIELDS = ("w_qkv", "w_fa", "w_fb", "w_ga", "w_gb", "w_beta", "w_o")
+
+
+def make_layer_weights(shape: Shape, d_model: int, rank: int, seed: int = 0,
+                       layer: int = 0) -> LayerWeights:
+    """Each weight ~ N(0, 1/fan_in), rounded to bf16, so unit-variance inputs give
+    unit-variance rows: the step sees q/k/v/f/beta/z of the distributions above."""
+    s = shape
+
+    def w(name, rows, cols):
+        x = normal(stream_key(seed, "proj", name, layer), rows * cols) / math.sqrt(cols)
+        return round_bf16(_f32(x, (rows, cols)))
+
+    return LayerWeights(d_model, rank,
+                        w("qkv", s.C, d_model), w("fa", rank, d_model),
+                        w("fb", s.H_v * s.d_k, rank), w("ga", rank, d_model),
+                        w("gb", s.H_v * s.d_v, rank), w("beta", s.H_v, d_model),
+                        w("o", d_model, s.H_v * s.d_v))
+
+
+def make_layer_input(shape: Shape, d_model: int, seed: int = 0, layer: int = 0,
+                     step: int = 0) -> np.ndarray:
+    """Layer input rows [B, d_model] ~ N(0, 1), rounded to bf16."""
+    return round_bf16(_f32(normal(stream_key(seed, "layer_x", layer, step), shape.B * d_model),
+                           (shape.B, d_model)))
+
+
 def with_tokens(shape: Shape, T: int, B: Optional[int] = None) -> Shape:
     return dataclasses.replace(shape, T=T, B=shape.B if B is None else B)

@@ -193,3 +193,30 @@ def test_product_path_never_touches_the_oracle():
                 assert "gdn_oracle" not in text, fn
     src = open(os.path.join(ROOT, "oracle", "gdn_oracle.c")).read()
     assert not re.search(r'#include\s+"', src), "oracle includes a local header"
+
+
+def test_layer_decode_argument_checks(lib):
+    """gdn_layer_decode refuses, before any launch: the per-head gate, bf16 rows,
+    T != 1, missing weights, a short workspace and misaligned rows."""
+    def weights(**kw):
+        base = dict(d_model=512, rank=32, w_qkv=0x100000, w_fa=0x110000, w_fb=0x120000,
+                    w_ga=0x130000, w_gb=0x140000, w_beta=0x150000, w_o=0x160000)
+        base.update(kw)
+        return gdn.GdnLayerWeights(**base)
+
+    def call(s, w, x=0x170000, x_out=0x180000, t=None, ws=0x190000, ws_bytes=1 << 20):
+        t = t or _tensors()
+        return lib.gdn_layer_decode(ctypes.byref(s), ctypes.byref(w), x, x_out, ctypes.byref(t),
+                                    ws, ws_bytes, None)
+
+    f32 = dict(bf16_in=False)
+    s = _shape(**f32)
+    assert gdn.gdn_layer_workspace_bytes(s, weights()) == 2 * 2 * 32 * 4
+    assert call(_shape(kda=False, **f32), weights()) == gdn.GDN_ERR_SHAPE
+    assert call(_shape(), weights()) == gdn.GDN_ERR_SHAPE          # bf16 rows
+    assert call(_shape(T=2, **f32), weights()) == gdn.GDN_ERR_SHAPE
+    assert call(s, weights(w_fb=0)) == gdn.GDN_ERR_NULL
+    assert call(s, weights(rank=12)) == gdn.GDN_ERR_SHAPE
+    assert call(s, weights(), ws_bytes=100) == gdn.GDN_ERR_WORKSPACE
+    assert call(s, weights(), x=0x170008) == gdn.GDN_ERR_ALIGN
+    assert call(s, weights(w_o=0x160004)) == gdn.GDN_ERR_ALIGN

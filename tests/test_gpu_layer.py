@@ -1,0 +1,73 @@
+"""A whole KDA layer's decode step (gdn_layer_decode: the projections around the
+step in four launches) against the oracle's projections and step."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_decode_kda_gb300 as gdn
+import synth
+from synth import device as dev
+
+from gpu_harness import DECODE_TOL, assert_close, stream
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+ROW_TOL = 2e-5  # fp32 projections against fp64, relative to the rows' RMS
+
+
+def _run(shape, d_model, rank, seed):
+    s = dataclasses.replace(shape, bf16_in=False)
+    params = synth.make_params(s, seed=seed)
+    state = synth.make_state(s, seed=seed)
+    W = synth.make_layer_weights(s, d_model, rank, seed=seed)
+    x = synth.make_layer_input(s, d_model, seed=seed)
+    zero = synth.Inputs(np.zeros((s.B, 1, s.C), np.float32),
+                        np.zeros((s.B, 1, s.H_v, s.d_k), np.float32),
+                        np.zeros((s.B, 1, s.H_v), np.float32),
+                        np.zeros((s.B, 1, s.H_v, s.d_v), np.float32))
+    case = dev.upload(s, params, zero, state)
+    sh = case.abi_shape()
+    wd = {k: dev.to_torch(getattr(W, k), True, "cuda") for k in W.FIELDS}
+    wts = gdn.layer_weights_from_torch(d_model, rank, **wd)
+    xs = dev.to_torch(x, True, "cuda")
+    x_out = torch.empty((s.B, d_model), dtype=torch.float32, device="cuda")
+    n = gdn.gdn_layer_workspace_bytes(sh, wts)
+    assert n == s.B * 2 * rank * 4
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    gdn.gdn_layer_decode(sh, wts, xs, x_out, case.abi_tensors(), ws.data_ptr(), n, stream())
+    torch.cuda.synchronize()
+    gdn.gdn_device_status()
+    ref = oracle.layer_decode(s, params, W, x, state.conv, state.S)
+    r = ref["rows"]
+    assert_close(case.qkv.reshape(s.B, -1), r["qkv"], ROW_TOL, "qkv rows")
+    assert_close(case.f.reshape(s.B, -1), r["f"], ROW_TOL, "f rows")
+    assert_close(case.beta.reshape(s.B, -1), r["beta"], ROW_TOL, "beta rows")
+    assert_close(case.z.reshape(s.B, -1), r["z"], ROW_TOL, "z rows")
+    assert_close(case.out.reshape(ref["y"].shape), ref["y"], DECODE_TOL, "y")
+    assert_close(x_out, ref["x_out"], DECODE_TOL, "x_out")
+    assert_close(case.state, ref["state"], DECODE_TOL, "state")
+    assert_close(case.conv_state, ref["conv_state"], ROW_TOL, "conv_state")
+
+
+@pytest.mark.parametrize("B", [1, 3, 9])
+def test_layer_decode_small(B):
+    """B = 9 takes two passes over each weight row (8 batch rows a pass)."""
+    shape = synth.Shape(B=B, T=1, H_qk=4, H_v=4, d_k=128, d_v=128, kda=True)
+    _run(shape, 512, 32, seed=60 + B)
+
+
+def test_layer_decode_grouped_heads_bounded_gate():
+    shape = synth.Shape(B=2, T=1, H_qk=2, H_v=4, d_k=128, d_v=128, kda=True, lb_gate=True,
+                        sigmoid_out=True)
+    _run(shape, 256, 16, seed=70)
+
+
+def test_layer_decode_b64_h32_d4096():
+    """The bench's batched layer: 64 sequences, 32 heads, d_model 4096, rank 128."""
+    shape = synth.Shape(B=64, T=1, H_qk=32, H_v=32, d_k=128, d_v=128, kda=True)
+    _run(shape, 4096, 128, seed=71)
