@@ -104,7 +104,7 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-template <bool BF16>
+template <bool BF16, bool PER_CHANNEL>
 __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned char *ws)
 {
     // staging rows of q, k, v and G; they take the block image at the end
@@ -237,6 +237,22 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
             // two channels at a time on the packed fp32 pipe
             float2 kk2 = make_float2(0.f, 0.f), qk2 = kk2;
             const float2 neg1 = make_float2(-1.f, -1.f);
+            if (!PER_CHANNEL) {
+                // one decay per head: e^{G_t - G_s} factors out of the channel sums
+#pragma unroll 4
+                for (int m = 0; m < 64; m += 4) {
+                    const float4 k1 = *reinterpret_cast<const float4 *>(&ks[t][base + m]);
+                    const float4 k0 = *reinterpret_cast<const float4 *>(&ks[s][base + m]);
+                    const float4 q1 = *reinterpret_cast<const float4 *>(&qs[t][base + m]);
+                    kk2 = __ffma2_rn(lo2(k1), lo2(k0), kk2);
+                    qk2 = __ffma2_rn(lo2(q1), lo2(k0), qk2);
+                    kk2 = __ffma2_rn(hi2(k1), hi2(k0), kk2);
+                    qk2 = __ffma2_rn(hi2(q1), hi2(k0), qk2);
+                }
+                const float e = ex2(gs[t][0] - gs[s][0]);
+                kk2 = make_float2(kk2.x * e, kk2.y * e);
+                qk2 = make_float2(qk2.x * e, qk2.y * e);
+            } else
 #pragma unroll 4
             for (int m = 0; m < 64; m += 4) {
                 const float4 g1 = *reinterpret_cast<const float4 *>(&gs[t][base + m]);
@@ -350,6 +366,7 @@ struct StateShared {
     uint64_t full[NSTG];
     uint64_t mma_bar;
     uint32_t tmem;
+    int fail;  // a bounded wait gave up somewhere in the CTA
 };
 
 // Makes this thread's shared-memory writes visible to the tensor core, then syncs the CTA.
@@ -360,16 +377,32 @@ __device__ __forceinline__ void publish_smem()
     __syncthreads();
 }
 
-// Thread layout: ch = tid % 128 is the state column j (TMEM lane j, warp w
-// reaching lanes 32 (w % 4) ..); half = tid / 128 splits the row-wise work.
-__global__ void __launch_bounds__(256, 1)
+constexpr int CT = 256;           // compute threads (8 warps)
+constexpr int ST_THREADS = CT + 32;  // plus the issuing warp
+constexpr int ISSUER_WARP = CT / 32;
+
+// Named barrier of the 256 compute threads (the norm's partial sums).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The CTA-wide barrier, taken by the compute warps and the issuing warp alike.
+__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 0;" ::: "memory"); }
+
+// A shared-memory descriptor moved `bytes` further (the start address sits in
+// bits 0-13 in 16-byte units; every operand here lies below 256 KiB).
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// Warps 0-7: ch = tid % 128 is the state column j (TMEM lane j, warp w reaching
+// lanes 32 (w % 4) ..); half = tid / 128 splits the row-wise work.  Warp 8 issues
+// every copy and every product, with descriptors computed once, so issuing never
+// sits on the compute warps' path.
+__global__ void __launch_bounds__(ST_THREADS, 1)
 kda_state_kernel(StepArgs a, const unsigned char *ws, int nchunk, const __grid_constant__ CUtensorMap tmz)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ __align__(16) StateShared ps;
     const int h = blockIdx.x, b = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int ch = tid & (KD - 1), half = tid >> 7;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer = warp == ISSUER_WARP;
+    const int ch = tid & (KD - 1), half = (tid >> 7) & 1;
     const int lb = 32 * (warp & 3);
     const size_t head = static_cast<size_t>(b) * a.H_v + h;
     const unsigned char *blocks = ws + head * nchunk * static_cast<size_t>(BLOCK_BYTES);
@@ -381,202 +414,233 @@ kda_state_kernel(StepArgs a, const unsigned char *ws, int nchunk, const __grid_c
     if (tid == 0) {
         for (int s = 0; s < NSTG; ++s) mbar_init(&ps.full[s], 1);
         mbar_init(&ps.mma_bar, 1);
+        ps.fail = 0;
         fence_mbar_init();
     }
     tc::fence_before_sync();
-    __syncthreads();
+    cta_sync();
     tc::fence_after_sync();
     const uint32_t tm = ps.tmem;
-    const uint32_t zbytes = KC * KD * (a.in_bf16 ? 2u : 4u);
-    auto issue = [&](int n) {
-        const int s = n % NSTG;
-        mbar_expect_tx(&ps.full[s], BLOCK_BYTES + zbytes);
-        tma_load_1d(sm + s * STAGE, blocks + static_cast<size_t>(n) * BLOCK_BYTES, BLOCK_BYTES, &ps.full[s]);
-        // rows past the last token of the batch read as zero; rows of the next sequence are unused
-        tma_load_3d(sm + s * STAGE + STAGE_Z, &tmz, 0, h, b * a.T + n * KC, &ps.full[s]);
-    };
-    // thread 128 (warp 4) issues every copy and every product
-    constexpr int ISSUER = 128;
-    if (tid == ISSUER) {
-        prefetch_tensormap(&tmz);
-        for (int n = 0; n < NSTG && n < nchunk; ++n) issue(n);
-    }
-
-    // state S[i][j] -> TMEM S^T and its split operand; half 0 takes rows i < 64
-    {
-        const float *Sg = a.state_in + head * KD * KD;
-        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
-            float v[16];
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) v[ii] = Sg[(i0 + ii) * KD + ch];
-            tc::tmem_st16(tc::taddr(tm, lb, TM_S + i0), v);
-            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0, KD), v);
-            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, KD), v + 8);
-        }
-    }
-    publish_smem();
-
-    const float nw = a.norm_w[ch];
     bool ok = true;
-    uint32_t mma_ph = 0;
-    auto mma_wait = [&]() {
-        if (ok) ok = mbar_wait_bounded(&ps.mma_bar, mma_ph);
-        mma_ph ^= 1u;
-        tc::fence_after_sync();
-    };
-    const uint32_t id16 = tc::idesc_f16(128, KC, false), id32 = tc::idesc_f16(128, 2 * KC, false),
-                   id128 = tc::idesc_f16(128, KD, false);
-    // 1. [P | Q']^T = S^T [W; e^G Q]^T of chunk n (one N = 32 product), issued once its
-    // block is in and S^T's operand is current
-    auto issue_p = [&](int n) {
-        const unsigned char *Bn = sm + (n % NSTG) * STAGE;
-        if (ok) ok = mbar_wait_bounded(&ps.full[n % NSTG], static_cast<uint32_t>((n / NSTG) & 1));
-        tc::fence_after_sync();
-        tc::mma_split(tm + TM_P, tc::smem_u32(st_hi), tc::smem_u32(st_lo), tc::smem_u32(Bn + BW_WQ),
-                      tc::smem_u32(Bn + BW_WQ + 8192), KD, id32, false);
-        tc::mma_commit(&ps.mma_bar);
-    };
-    if (tid == ISSUER) issue_p(0);
 
-#pragma unroll 1
-    for (int n = 0; n < nchunk; ++n) {
-        const int t0 = n * KC, nt = min(KC, a.T - t0);
-        const unsigned char *B = sm + (n % NSTG) * STAGE;
-        if (ok) ok = mbar_wait_bounded(&ps.full[n % NSTG], static_cast<uint32_t>((n / NSTG) & 1));
-        mma_wait();  // P^T of this chunk
-
-        // 2. V_new = U - P as the split operand V_new^T; S^T <- e^{G_last} S^T by state row
-        if (half == 0) {
-            float p[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_P), p);
-            const float *U = reinterpret_cast<const float *>(B + BW_U);
+    if (issuer) {
+        const uint32_t zbytes = KC * KD * (a.in_bf16 ? 2u : 4u);
+        auto issue = [&](int n) {
+            const int s = n % NSTG;
+            mbar_expect_tx(&ps.full[s], BLOCK_BYTES + zbytes);
+            tma_load_1d(sm + s * STAGE, blocks + static_cast<size_t>(n) * BLOCK_BYTES, BLOCK_BYTES, &ps.full[s]);
+            // rows past the last token of the batch read as zero; rows of the next sequence are unused
+            tma_load_3d(sm + s * STAGE + STAGE_Z, &tmz, 0, h, b * a.T + n * KC, &ps.full[s]);
+        };
+        // descriptors: S^T (A, K = 128) and stage 0's [W; e^G Q] (B, K = 128); the
+        // K = 16 operands V_new^T (A), A (B) and (e^{G_last-G} K)^T (B)
+        uint64_t dsh[8], dsl[8], dwh[8], dwl[8];
 #pragma unroll
-            for (int t = 0; t < KC; ++t) p[t] = U[t * KD + ch] - p[t];
-            tc::put_row8(vn_hi, vn_lo, tc::op_offset(ch, 0, KC), p);
-            tc::put_row8(vn_hi, vn_lo, tc::op_offset(ch, 8, KC), p + 8);
+        for (int i = 0; i < 8; ++i) {
+            dsh[i] = tc::op_desc(tc::smem_u32(st_hi), 16 * i, KD);
+            dsl[i] = tc::op_desc(tc::smem_u32(st_lo), 16 * i, KD);
+            dwh[i] = tc::op_desc(tc::smem_u32(sm + BW_WQ), 16 * i, KD);
+            dwl[i] = tc::op_desc(tc::smem_u32(sm + BW_WQ + 8192), 16 * i, KD);
         }
-        {
-            const float *gl = reinterpret_cast<const float *>(B + BW_G);
-            for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
-                float sv[16];
-                tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
+        const uint64_t dvh = tc::op_desc(tc::smem_u32(vn_hi), 0, KC), dvl = tc::op_desc(tc::smem_u32(vn_lo), 0, KC);
+        const uint64_t dmh = tc::op_desc(tc::smem_u32(sm + BW_M), 0, KC),
+                       dml = tc::op_desc(tc::smem_u32(sm + BW_M + 512), 0, KC);
+        const uint64_t dkh = tc::op_desc(tc::smem_u32(sm + BW_K), 0, KC),
+                       dkl = tc::op_desc(tc::smem_u32(sm + BW_K + 4096), 0, KC);
+        const uint32_t id16 = tc::idesc_f16(128, KC, false), id32 = tc::idesc_f16(128, 2 * KC, false),
+                       id128 = tc::idesc_f16(128, KD, false);
+        // 1. [P | Q']^T = S^T [W; e^G Q]^T of chunk n (one N = 32 product, split operands)
+        auto issue_p = [&](int n) {
+            const uint32_t so = (n % NSTG) * STAGE;
+            if (ok) ok = mbar_wait_bounded(&ps.full[n % NSTG], static_cast<uint32_t>((n / NSTG) & 1));
+            tc::fence_after_sync();
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) sv[ii] *= gl[i0 + ii];
-                tc::tmem_st16(tc::taddr(tm, lb, TM_S + i0), sv);
+            for (int i = 0; i < 8; ++i) tc::mma_f16(tm + TM_P, dsh[i], desc_at(dwh[i], so), id32, i > 0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tc::mma_f16(tm + TM_P, dsh[i], desc_at(dwl[i], so), id32, true);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tc::mma_f16(tm + TM_P, dsl[i], desc_at(dwh[i], so), id32, true);
+            tc::mma_commit(&ps.mma_bar);
+        };
+        // 3. O^T = Q'^T + V_new^T A^T;  S^T += V_new^T (e^{G_last - G} K)
+        auto issue_o = [&](int n) {
+            const uint32_t so = (n % NSTG) * STAGE;
+            tc::fence_after_sync();
+            tc::mma_f16(tm + TM_O, dvh, desc_at(dmh, so), id16, true);
+            tc::mma_f16(tm + TM_O, dvh, desc_at(dml, so), id16, true);
+            tc::mma_f16(tm + TM_O, dvl, desc_at(dmh, so), id16, true);
+            tc::mma_f16(tm + TM_S, dvh, desc_at(dkh, so), id128, true);
+            tc::mma_f16(tm + TM_S, dvh, desc_at(dkl, so), id128, true);
+            tc::mma_f16(tm + TM_S, dvl, desc_at(dkh, so), id128, true);
+            tc::mma_commit(&ps.mma_bar);
+        };
+        if (lane == 0) {
+            prefetch_tensormap(&tmz);
+            for (int n = 0; n < NSTG && n < nchunk; ++n) issue(n);
+        }
+        cta_sync();  // S^T and its operand are in
+        if (lane == 0) issue_p(0);
+#pragma unroll 1
+        for (int n = 0; n < nchunk; ++n) {
+            cta_sync();  // V_new^T and the decayed S^T are in
+            if (lane == 0) issue_o(n);
+            cta_sync();  // the stage is consumed; the new S^T operand is in
+            if (lane == 0) {
+                if (n + NSTG < nchunk) issue(n + NSTG);
+                if (n + 1 < nchunk) issue_p(n + 1);  // overlaps the norm and the stores
+            }
+        }
+        if (!ok) ps.fail = 1;
+    } else {
+        // state S[i][j] -> TMEM S^T and its split operand; half 0 takes rows i < 64
+        {
+            const float *Sg = a.state_in + head * KD * KD;
+            for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) v[ii] = Sg[(i0 + ii) * KD + ch];
+                tc::tmem_st16(tc::taddr(tm, lb, TM_S + i0), v);
+                tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0, KD), v);
+                tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, KD), v + 8);
             }
         }
         publish_smem();
 
-        // 3. O^T = Q'^T + V_new^T A^T;  S^T += V_new^T (e^{G_last - G} K)
-        if (tid == ISSUER) {
+        const float nw = a.norm_w[ch];
+        uint32_t mma_ph = 0;
+        auto mma_wait = [&]() {
+            if (ok) ok = mbar_wait_bounded(&ps.mma_bar, mma_ph);
+            mma_ph ^= 1u;
             tc::fence_after_sync();
-            const uint32_t vh = tc::smem_u32(vn_hi), vl = tc::smem_u32(vn_lo);
-            tc::mma_split(tm + TM_O, vh, vl, tc::smem_u32(B + BW_M), tc::smem_u32(B + BW_M + 512), KC,
-                          id16, true);
-            tc::mma_split(tm + TM_S, vh, vl, tc::smem_u32(B + BW_K), tc::smem_u32(B + BW_K + 4096), KC,
-                          id128, true);
-            tc::mma_commit(&ps.mma_bar);
-        }
-        mma_wait();
+        };
 
-        // 4. each half: o, its squares and the output gate of tokens 8 half .. +7, and
-        // the new S^T of rows 64 half .. +63 as the next chunk's operand
-        float o[8], gz[8];
-        tc::tmem_ld8(tc::taddr(tm, lb, TM_O + 8 * half), o);
+#pragma unroll 1
+        for (int n = 0; n < nchunk; ++n) {
+            const int t0 = n * KC, nt = min(KC, a.T - t0);
+            const unsigned char *B = sm + (n % NSTG) * STAGE;
+            if (ok) ok = mbar_wait_bounded(&ps.full[n % NSTG], static_cast<uint32_t>((n / NSTG) & 1));
+            mma_wait();  // [P | Q']^T of this chunk
+
+            // 2. V_new = U - P as the split operand V_new^T; S^T <- e^{G_last} S^T by state row
+            if (half == 0) {
+                float p[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_P), p);
+                const float *U = reinterpret_cast<const float *>(B + BW_U);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int t = 8 * half + j;
-            sq[t * SQS + ch] = o[j] * o[j];
-            const float zz = a.in_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(B + STAGE_Z)[t * KD + ch])
-                                       : reinterpret_cast<const float *>(B + STAGE_Z)[t * KD + ch];
-            gz[j] = nw * (a.sig_gate ? fast_sigmoid(zz) : fast_silu(zz));
-        }
-        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
-            float sv[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
-            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0, KD), sv);
-            tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, KD), sv + 8);
-        }
-        publish_smem();  // the stage is consumed; o^2 and the S^T operand are in
+                for (int t = 0; t < KC; ++t) p[t] = U[t * KD + ch] - p[t];
+                tc::put_row8(vn_hi, vn_lo, tc::op_offset(ch, 0, KC), p);
+                tc::put_row8(vn_hi, vn_lo, tc::op_offset(ch, 8, KC), p + 8);
+            }
+            {
+                const float *gl = reinterpret_cast<const float *>(B + BW_G);
+                for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+                    float sv[16];
+                    tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
+#pragma unroll
+                    for (int ii = 0; ii < 16; ++ii) sv[ii] *= gl[i0 + ii];
+                    tc::tmem_st16(tc::taddr(tm, lb, TM_S + i0), sv);
+                }
+            }
+            publish_smem();
+            mma_wait();  // O^T and the new S^T
 
-        // 5. gated RMSNorm over the 128 columns of each token (16 threads a token)
+            // 4. each half: o, its squares and the output gate of tokens 8 half .. +7, and
+            // the new S^T of rows 64 half .. +63 as the next chunk's operand
+            float o[8], gz[8];
+            tc::tmem_ld8(tc::taddr(tm, lb, TM_O + 8 * half), o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = 8 * half + j;
+                sq[t * SQS + ch] = o[j] * o[j];
+                const float zz = a.in_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(B + STAGE_Z)[t * KD + ch])
+                                           : reinterpret_cast<const float *>(B + STAGE_Z)[t * KD + ch];
+                gz[j] = nw * (a.sig_gate ? fast_sigmoid(zz) : fast_silu(zz));
+            }
+            for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+                float sv[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
+                tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0, KD), sv);
+                tc::put_row8(st_hi, st_lo, tc::op_offset(ch, i0 + 8, KD), sv + 8);
+            }
+            publish_smem();  // the stage is consumed; o^2 and the S^T operand are in
+
+            // 5. gated RMSNorm over the 128 columns of each token (16 threads a token)
+            {
+                const int t = tid >> 4, part = tid & 15;
+                float s_ = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s_ += sq[t * SQS + 8 * part + j];
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 1);
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 2);
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 4);
+                s_ += __shfl_xor_sync(0xffffffffu, s_, 8);
+                if (part == 0) ps.rinv[t] = 1.0f / sqrtf(s_ / static_cast<float>(KD) + a.eps_norm);
+            }
+            compute_sync();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = 8 * half + j;
+                if (t < nt) {
+                    const size_t idx = ((static_cast<size_t>(b) * a.T + t0 + t) * a.H_v + h) * KD + ch;
+                    const float yv = o[j] * ps.rinv[t] * gz[j];
+                    if (a.out_bf16)
+                        reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(yv);
+                    else
+                        reinterpret_cast<float *>(a.out)[idx] = yv;
+                }
+            }
+        }
+
+        // final state S[i][j] from S^T (lane j)
         {
-            const int t = tid >> 4, part = tid & 15;
-            float s_ = 0.f;
+            float *So = a.state_out + head * KD * KD;
+            for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
+                float sv[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s_ += sq[t * SQS + 8 * part + j];
-            s_ += __shfl_xor_sync(0xffffffffu, s_, 1);
-            s_ += __shfl_xor_sync(0xffffffffu, s_, 2);
-            s_ += __shfl_xor_sync(0xffffffffu, s_, 4);
-            s_ += __shfl_xor_sync(0xffffffffu, s_, 8);
-            if (part == 0) ps.rinv[t] = 1.0f / sqrtf(s_ / static_cast<float>(KD) + a.eps_norm);
-        }
-        __syncthreads();
-        if (tid == ISSUER) {
-            if (n + NSTG < nchunk) issue(n + NSTG);
-            if (n + 1 < nchunk) issue_p(n + 1);  // overlaps this chunk's output rows
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int t = 8 * half + j;
-            if (t < nt) {
-                const size_t idx = ((static_cast<size_t>(b) * a.T + t0 + t) * a.H_v + h) * KD + ch;
-                const float yv = o[j] * ps.rinv[t] * gz[j];
-                if (a.out_bf16)
-                    reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(yv);
-                else
-                    reinterpret_cast<float *>(a.out)[idx] = yv;
+                for (int ii = 0; ii < 16; ++ii) So[(i0 + ii) * KD + ch] = sv[ii];
             }
         }
-    }
-
-    // final state S[i][j] from S^T (lane j)
-    {
-        float *So = a.state_out + head * KD * KD;
-        for (int i0 = 64 * half; i0 < 64 * half + 64; i0 += 16) {
-            float sv[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), sv);
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) So[(i0 + ii) * KD + ch] = sv[ii];
-        }
-    }
-    // final conv window: rows T, T+1, T+2 of [kept window; the T new rows].  v
-    // channels by their head, q and k channels by the group's first value head
-    {
-        const int hq = h / a.group;
-        const size_t C = static_cast<size_t>(a.C);
-        int chn[2], nc = 0;
-        if (half == 0) {
-            chn[nc++] = 2 * a.H_qk * KD + h * KD + ch;
-        } else if (h % a.group == 0) {
-            chn[nc++] = hq * KD + ch;
-            chn[nc++] = a.H_qk * KD + hq * KD + ch;
-        }
-        for (int m = 0; m < nc; ++m) {
-            const int c = chn[m];
-            float x3[3];
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-                const int idx = a.T + j;
-                x3[j] = idx < 3 ? a.conv_in[(static_cast<size_t>(b) * 3 + idx) * C + c]
-                                : ld_in(a.qkv, (static_cast<size_t>(b) * a.T + idx - 3) * C + c, a.in_bf16);
+        // final conv window: rows T, T+1, T+2 of [kept window; the T new rows].  v
+        // channels by their head, q and k channels by the group's first value head
+        {
+            const int hq = h / a.group;
+            const size_t C = static_cast<size_t>(a.C);
+            int chn[2], nc = 0;
+            if (half == 0) {
+                chn[nc++] = 2 * a.H_qk * KD + h * KD + ch;
+            } else if (h % a.group == 0) {
+                chn[nc++] = hq * KD + ch;
+                chn[nc++] = a.H_qk * KD + hq * KD + ch;
             }
+            for (int m = 0; m < nc; ++m) {
+                const int c = chn[m];
+                float x3[3];
 #pragma unroll
-            for (int j = 0; j < 3; ++j) a.conv_out[(static_cast<size_t>(b) * 3 + j) * C + c] = x3[j];
+                for (int j = 0; j < 3; ++j) {
+                    const int idx = a.T + j;
+                    x3[j] = idx < 3 ? a.conv_in[(static_cast<size_t>(b) * 3 + idx) * C + c]
+                                    : ld_in(a.qkv, (static_cast<size_t>(b) * a.T + idx - 3) * C + c, a.in_bf16);
+                }
+#pragma unroll
+                for (int j = 0; j < 3; ++j) a.conv_out[(static_cast<size_t>(b) * 3 + j) * C + c] = x3[j];
+            }
         }
+        if (!ok) ps.fail = 1;
     }
-    if (!ok && tid == ISSUER) {
+    cta_sync();
+    if (ps.fail && tid == ISSUER_WARP * 32) {
         // a wait gave up: let the copies and products still in flight land
         // (bounded) before the shared memory and TMEM are released
         for (int s = 0; s < NSTG && s < nchunk; ++s) {
             const int last = s + NSTG * ((nchunk - 1 - s) / NSTG);
             mbar_wait_bounded(&ps.full[s], static_cast<uint32_t>((last / NSTG) & 1));
         }
-        mbar_wait_bounded(&ps.mma_bar, mma_ph ^ 1u);
+        mbar_wait_bounded(&ps.mma_bar, static_cast<uint32_t>((2 * nchunk - 1) & 1));
         atomicOr(&g_kda_error, 1u);
     }
     tc::fence_before_sync();
-    __syncthreads();
+    cta_sync();
     if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
 }
 
@@ -624,13 +688,18 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
                           a.z, dim, stride, box))
             return cudaErrorInvalidValue;
     }
-    if (a.in_bf16)
-        kda_intra_kernel<true><<<dim3(nchunk, a.H_v, a.B), 256, 0, stream>>>(a, ws);
+    const dim3 grid(nchunk, a.H_v, a.B);
+    if (a.in_bf16 && a.kda)
+        kda_intra_kernel<true, true><<<grid, 256, 0, stream>>>(a, ws);
+    else if (a.in_bf16)
+        kda_intra_kernel<true, false><<<grid, 256, 0, stream>>>(a, ws);
+    else if (a.kda)
+        kda_intra_kernel<false, true><<<grid, 256, 0, stream>>>(a, ws);
     else
-        kda_intra_kernel<false><<<dim3(nchunk, a.H_v, a.B), 256, 0, stream>>>(a, ws);
+        kda_intra_kernel<false, false><<<grid, 256, 0, stream>>>(a, ws);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kda_state_kernel<<<dim3(a.H_v, a.B), 256, SMEM, stream>>>(a, ws, nchunk, tmz);
+    kda_state_kernel<<<dim3(a.H_v, a.B), ST_THREADS, SMEM, stream>>>(a, ws, nchunk, tmz);
     return cudaGetLastError();
 }
 
