@@ -84,15 +84,16 @@ def prefill_flops(s: synth.Shape) -> float:
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
-def kda_chunk_flops(s: synth.Shape, C: int = 16) -> float:
-    """fp32 FLOPs of the two-kernel chunked form at chunk C, per (sequence, value
-    head, chunk): W S, Q S and the state update (2 C d^2 each), A V_new (2 C^2 d),
-    the pair sums K K^T and Q K^T over the lower triangle (C^2 d each) and the
+def two_kernel_flops(s: synth.Shape, C: int = 16):
+    """(tensor, fp32) FLOPs of the two-kernel chunked form at chunk C, per
+    (sequence, value head, chunk): the state kernel's tcgen05 products W S, e^G Q S
+    and the state update (2 C d^2 each) and A V_new (2 C^2 d); the intra kernel's
+    fp32 pair sums K K^T and Q K^T over the lower triangle (C^2 d each) and the
     forward substitution on 2d columns (C^2 d each side)."""
     d = s.d_k
-    nch = -(-s.T // C)
-    per = 3 * 2 * C * d * d + 2 * C * C * d + 2 * C * C * d + 2 * C * C * d
-    return float(s.B * s.H_v * nch * per)
+    units = s.B * s.H_v * -(-s.T // C)
+    return (float(units * (3 * 2 * C * d * d + 2 * C * C * d)),
+            float(units * (2 * C * C * d + 2 * C * C * d)))
 
 
 def measured_peaks() -> dict:
@@ -333,7 +334,9 @@ class SingleLaunch(Workload):
         self.flops_per_launch = (prefill_flops(dataclasses.replace(s, chunk=int(m.group(1))))
                                  if m else 0.0)
         m = re.match(r"kda_chunked<(\d+)>", self.kernel or "") if op == gdn.OP_PREFILL else None
-        self.alu_flops_per_launch = kda_chunk_flops(s, int(m.group(1))) if m else 0.0
+        self.alu_flops_per_launch = 0.0
+        if m:
+            self.flops_per_launch, self.alu_flops_per_launch = two_kernel_flops(s, int(m.group(1)))
         self.ws_bytes = gdn.gdn_prefill_workspace_bytes(self.abi_shape) if op == 2 else 0
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         self.h2d_bytes = sum(v[0].numel() * v.element_size() for v in self.dev_in.values())

@@ -170,11 +170,11 @@ GDN_API gdn_status_t gdn_commit_accepted(const gdn_shape_t *shape, const gdn_ten
  * Chunked prefill of T >= 1 tokens per sequence: the same result as T decode
  * steps, computed in the chunked WY/UT form ("llama.cpp PR #84", chunked
  * KDA prefill).  conv_state and state are advanced in place; out receives y
- * for every token.  Per-head decay with bf16 rows at d = 128 runs the
- * tensor-core kernel in 32-token chunks (shape->chunk 32 or 64); the other
- * d = 128 shapes with T > 4 run the two-kernel form in 16-token chunks
- * (whatever shape->chunk asks, which must be > 0); the rest run the
- * recurrent kernel.  workspace must hold gdn_prefill_workspace_bytes(shape)
+ * for every token.  At d = 128 and T > 4 the two-kernel form runs (an
+ * intra-chunk pass over all 16-token chunks, then a tcgen05 state pass),
+ * whatever shape->chunk asks (which must be > 0), except that shape->chunk == 32
+ * with the per-head decay and bf16 rows runs the single tensor-core kernel in
+ * 32-token chunks; other shapes run the recurrent kernel.  workspace must hold gdn_prefill_workspace_bytes(shape)
  * bytes, 16-byte aligned (may be 0 bytes; then NULL is accepted); the call
  * owns it until the work queued on `stream` completes.
  */

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
     __shared__ __align__(16) float As[KC][KC];
     __shared__ float bs[KC];
     __shared__ float red[4][32];
+    __shared__ float rqk[2][KC];  // per token: q_scale / |q|, 1 / |k|
 
     const int n = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -177,6 +178,8 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         for (int t = 0; t < KC; ++t) {
             v[t] = q[t] * q[t];
             v[KC + t] = k[t] * k[t];
+            qs[t][hp(i)] = q[t];  // raw rows; the norms scale the products below
+            ks[t][hp(i)] = k[t];
         }
         red[warp][lane] = reduce_scatter32(v, lane);
     } else {
@@ -209,14 +212,9 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         }
     }
     __syncthreads();
-    if (tid < KD) {
-#pragma unroll
-        for (int t = 0; t < KC; ++t) {
-            const float sq = red[0][t] + red[1][t] + red[2][t] + red[3][t];
-            const float sk = red[0][KC + t] + red[1][KC + t] + red[2][KC + t] + red[3][KC + t];
-            qs[t][hp(i)] = q[t] * (a.q_scale / sqrtf(sq + a.eps_l2));
-            ks[t][hp(i)] = k[t] * (1.0f / sqrtf(sk + a.eps_l2));
-        }
+    if (tid < 32) {  // the L2 norms: lanes 0-15 q of token lane, 16-31 k of token lane - 16
+        const float sq = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
+        rqk[tid >> 4][tid & 15] = (tid < KC ? a.q_scale : 1.0f) / sqrtf(sq + a.eps_l2);
     }
     __syncthreads();
 
@@ -285,11 +283,11 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         const float qk2 = __shfl_xor_sync(0xffffffffu, qk, 1);
         if (tid < 240) {
             if ((tid & 1) == 0) {
-                Ls[t][s] = bs[t] * (kk + kk2);
-                As[t][s] = qk + qk2;
+                Ls[t][s] = bs[t] * (kk + kk2) * rqk[1][t] * rqk[1][s];
+                As[t][s] = (qk + qk2) * rqk[0][t] * rqk[1][s];
             }
         } else {
-            As[t][t] = qk;
+            As[t][t] = qk * rqk[0][t] * rqk[1][t];
         }
     }
     __syncthreads();
@@ -302,18 +300,28 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         const bool wside = tid < KD;
 #pragma unroll
         for (int t = 0; t < KC; ++t)
-            x[t] = bs[t] * (wside ? ks[t][hp(i)] * ex2(gs[t][hp(i)]) : vs[t][hp(i)]);
+            x[t] = bs[t] * (wside ? ks[t][hp(i)] * rqk[1][t] * ex2(gs[t][hp(i)]) : vs[t][hp(i)]);
 #pragma unroll
-        for (int t = 1; t < KC; ++t)
+        for (int t = 1; t < KC; ++t) {
+            float l[KC];
 #pragma unroll
-            for (int s = 0; s < t; ++s) x[t] = fmaf(-Ls[t][s], x[s], x[t]);
+            for (int s4 = 0; s4 < KC; s4 += 4) {
+                const float4 v4 = *reinterpret_cast<const float4 *>(&Ls[t][s4]);
+                l[s4] = v4.x;
+                l[s4 + 1] = v4.y;
+                l[s4 + 2] = v4.z;
+                l[s4 + 3] = v4.w;
+            }
+#pragma unroll
+            for (int s = 0; s < t; ++s) x[t] = fmaf(-l[s], x[s], x[t]);
+        }
         if (wside) {
 #pragma unroll
-            for (int t = 0; t < KC; ++t) y[t] = qs[t][hp(i)] * ex2(gs[t][hp(i)]);
+            for (int t = 0; t < KC; ++t) y[t] = qs[t][hp(i)] * rqk[0][t] * ex2(gs[t][hp(i)]);
         } else {
             const float Gl = gs[KC - 1][hp(i)];
 #pragma unroll
-            for (int t = 0; t < KC; ++t) y[t] = ks[t][hp(i)] * ex2(Gl - gs[t][hp(i)]);
+            for (int t = 0; t < KC; ++t) y[t] = ks[t][hp(i)] * rqk[1][t] * ex2(Gl - gs[t][hp(i)]);
             gl = ex2(Gl);
         }
     }

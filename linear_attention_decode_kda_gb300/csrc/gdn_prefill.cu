@@ -546,13 +546,15 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
     if (!ok && lane == 0) atomicOr(&g_prefill_error, 1u);
 }
 
-// Shapes the tensor-core kernel takes (its pointer rules aside).
+// Shapes the single tensor-core kernel takes (its pointer rules aside): the caller
+// asks for its 32-token chunks with chunk == 32; other chunk lengths take the
+// faster two-kernel form (gdn_kda_prefill.cu).
 bool chunked_shape(const gdn_shape_t &s)
 {
     const int group = s.H_v / s.H_qk;
     const size_t C = 2 * static_cast<size_t>(s.H_qk) * s.d_k + static_cast<size_t>(s.H_v) * s.d_v;
     return s.gate_mode == GDN_GATE_PER_HEAD && s.d_k == PD && s.d_v == PD &&
-           s.in_dtype == GDN_BF16 && (s.chunk == CH || s.chunk == 64) && group <= 8 &&
+           s.in_dtype == GDN_BF16 && s.chunk == CH && group <= 8 &&
            (C * 2) % 16 == 0 && static_cast<long long>(s.B) * s.T < (1LL << 31);
 }
 

@@ -200,16 +200,20 @@ def _prefill(shape, seed=0, slow=False, tol=PREFILL_TOL, bf16_out=False, variant
 
 @pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200])
 def test_prefill_ragged_lengths(T):
-    shape = synth.Shape(B=2, T=T, H_qk=4, H_v=8, d_k=128, d_v=128, kda=False, chunk=64)
+    """The single tensor-core kernel (chunk 32), and the two-kernel form (chunk 64)."""
+    shape = synth.Shape(B=2, T=T, H_qk=4, H_v=8, d_k=128, d_v=128, kda=False, chunk=32)
     _prefill(shape, slow=True, variant="chunked<128,32>")
+    _prefill(dataclasses.replace(shape, chunk=64), slow=True,
+             variant="kda_chunked<16>" if T > 4 else None)
 
 
 @pytest.mark.parametrize("H_qk,H_v", [(4, 4), (2, 8)])
 def test_prefill_chunked_head_groups(H_qk, H_v):
     """Ungrouped heads and four value heads per qk head (thread-block cluster of 4)."""
-    shape = synth.Shape(B=3, T=130, H_qk=H_qk, H_v=H_v, d_k=128, d_v=128, kda=False, chunk=64)
+    shape = synth.Shape(B=3, T=130, H_qk=H_qk, H_v=H_v, d_k=128, d_v=128, kda=False, chunk=32)
     _prefill(shape, seed=5, variant="chunked<128,32>")
     _prefill(shape, seed=6, slow=True)
+    _prefill(dataclasses.replace(shape, chunk=64), seed=6, slow=True, variant="kda_chunked<16>")
 
 
 def test_prefill_chunked_bf16_out():
