@@ -104,11 +104,21 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
+// bf16 rows t0 - 3 .. t0 + 15 of one head's q, k and v channels: three TMA
+// boxes of 19 rows x 128 channels, then the chunk's 16 gate rows (per-channel
+// gates), laid over the staging rows until the conv has read them.
+constexpr int RAW_ROWS = KC + 3;
+constexpr int RAW_SEG = RAW_ROWS * KD * 2;  // bytes of one box (a multiple of 128)
+static_assert(RAW_SEG % 128 == 0, "TMA destinations 128-byte aligned");
+
 template <bool BF16, bool PER_CHANNEL>
-__global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned char *ws)
+__global__ void __launch_bounds__(256, 4)
+kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensorMap tq,
+                 const __grid_constant__ CUtensorMap tf)
 {
     // staging rows of q, k, v and G; they take the block image at the end
     __shared__ __align__(128) float stg[4][KC][SP];
+    __shared__ uint64_t raw_bar;
     float(*qs)[SP] = stg[0];
     float(*ks)[SP] = stg[1];
     float(*vs)[SP] = stg[2];
@@ -159,40 +169,86 @@ __global__ void __launch_bounds__(256, 4) kda_intra_kernel(StepArgs a, unsigned 
         }
     };
 
+    // bf16 rows by TMA; fp32 rows (and the per-head gate) by plain loads
+    const unsigned char *raw = reinterpret_cast<const unsigned char *>(&stg[0][0][0]);
+    const int chq = hq * KD, chk = a.H_qk * KD + hq * KD, chv = 2 * a.H_qk * KD + h * KD;
+    if (BF16) {
+        if (tid == 0) {
+            mbar_init(&raw_bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            unsigned char *dst = reinterpret_cast<unsigned char *>(&stg[0][0][0]);
+            const int row = b * a.T + t0 - 3;  // rows before the batch read as zero
+            mbar_expect_tx(&raw_bar, 3 * RAW_SEG + (PER_CHANNEL ? KC * KD * 2 : 0));
+            tma_load_2d(dst, &tq, chq, row, &raw_bar);
+            tma_load_2d(dst + RAW_SEG, &tq, chk, row, &raw_bar);
+            tma_load_2d(dst + 2 * RAW_SEG, &tq, chv, row, &raw_bar);
+            if (PER_CHANNEL) tma_load_3d(dst + 3 * RAW_SEG, &tf, 0, h, b * a.T + t0, &raw_bar);
+        }
+    }
+    // channel i of box sg: rows t0 - 3 .. t0 + 15, the first three from the kept
+    // window at the sequence's start
+    auto box_rows = [&](int sg, int c, float(&x)[KC + 3]) {
+        const __nv_bfloat16 *r = reinterpret_cast<const __nv_bfloat16 *>(raw + sg * RAW_SEG) + i;
+#pragma unroll
+        for (int j = 0; j < KC + 3; ++j) x[j] = __bfloat162float(r[j * KD]);
+        if (t0 == 0)
+#pragma unroll
+            for (int j = 0; j < 3; ++j) x[j] = a.conv_in[(static_cast<size_t>(b) * 3 + j) * C + c];
+    };
+
     // ---- 1. conv, squares for the L2 norms, gates; padded tokens are zero
     if (tid < KC) bs[tid] = tid < nt ? fast_sigmoid(ld(a.beta, (row0 + tid) * a.H_v + h)) : 0.f;
     Ls[tid >> 4][tid & 15] = 0.f;
     As[tid >> 4][tid & 15] = 0.f;
-    float q[KC], k[KC];
-    if (tid < KD) {
-        {
-            const int cq = hq * KD + i, ck = a.H_qk * KD + hq * KD + i;
-            float xq[KC + 3], xk[KC + 3];
-            load_rows(cq, xq);
-            load_rows(ck, xk);
-            conv_rows(cq, xq, q);
-            conv_rows(ck, xk, k);
-        }
-        float v[32];
-#pragma unroll
-        for (int t = 0; t < KC; ++t) {
-            v[t] = q[t] * q[t];
-            v[KC + t] = k[t] * k[t];
-            qs[t][hp(i)] = q[t];  // raw rows; the norms scale the products below
-            ks[t][hp(i)] = k[t];
-        }
-        red[warp][lane] = reduce_scatter32(v, lane);
-    } else {
-        const int cv = 2 * a.H_qk * KD + h * KD + i;
-        float xv[KC + 3], fl[KC];
-        load_rows(cv, xv);
+    float fl[KC];
+    if (tid >= KD && !(BF16 && PER_CHANNEL)) {
 #pragma unroll
         for (int t = 0; t < KC; ++t) {
             const size_t bth = (static_cast<size_t>(b) * a.T + min(t0 + t, a.T - 1)) * a.H_v + h;
-            fl[t] = a.kda ? ld(a.f, bth * KD + i) : ld(a.f, bth);
+            fl[t] = PER_CHANNEL ? ld(a.f, bth * KD + i) : ld(a.f, bth);
         }
-        float v[KC];
-        conv_rows(cv, xv, v);
+    }
+    if (BF16 && !mbar_wait_bounded(&raw_bar, 0)) atomicOr(&g_kda_error, 1u);
+    float q[KC], k[KC], v[KC];
+    if (tid < KD) {
+        float xq[KC + 3], xk[KC + 3];
+        if (BF16) {
+            box_rows(0, chq + i, xq);
+            box_rows(1, chk + i, xk);
+        } else {
+            load_rows(chq + i, xq);
+            load_rows(chk + i, xk);
+        }
+        conv_rows(chq + i, xq, q);
+        conv_rows(chk + i, xk, k);
+    } else {
+        float xv[KC + 3];
+        if (BF16) {
+            box_rows(2, chv + i, xv);
+            if (PER_CHANNEL)
+#pragma unroll
+                for (int t = 0; t < KC; ++t)
+                    fl[t] = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(raw + 3 * RAW_SEG)[t * KD + i]);
+        } else {
+            load_rows(chv + i, xv);
+        }
+        conv_rows(chv + i, xv, v);
+    }
+    if (BF16) __syncthreads();  // the rows are read: the staging rows take q, k, v, G
+    if (tid < KD) {
+        float sq2[32];
+#pragma unroll
+        for (int t = 0; t < KC; ++t) {
+            sq2[t] = q[t] * q[t];
+            sq2[KC + t] = k[t] * k[t];
+            qs[t][hp(i)] = q[t];  // raw rows; the norms scale the products below
+            ks[t][hp(i)] = k[t];
+        }
+        red[warp][lane] = reduce_scatter32(sq2, lane);
+    } else {
 #pragma unroll
         for (int t = 0; t < KC; ++t) vs[t][hp(i)] = v[t];
         // log-decays of channel i summed along the chunk, in log2 units.  Softplus
@@ -662,7 +718,9 @@ bool kda_chunk_shape(const gdn_shape_t &s)
 
 bool kda_chunk_pointers_ok(const StepArgs &a)
 {
-    return (reinterpret_cast<uintptr_t>(a.z) & 15u) == 0;  // the output-gate rows go by TMA
+    // z goes by TMA; so do bf16 q/k/v rows and per-channel gate rows
+    const auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    return al16(a.z) && (!a.in_bf16 || (al16(a.qkv) && (!a.kda || al16(a.f))));
 }
 
 size_t kda_chunk_workspace_bytes(const gdn_shape_t &s)
@@ -696,15 +754,32 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
                           a.z, dim, stride, box))
             return cudaErrorInvalidValue;
     }
+    CUtensorMap tq = {}, tf = {};
+    if (a.in_bf16) {
+        {   // qkv as [B*T rows][C channels], boxes of 19 rows x 128 channels
+            const uint64_t dim[2] = {static_cast<uint64_t>(a.C), static_cast<uint64_t>(a.B) * a.T};
+            const uint64_t stride[1] = {static_cast<uint64_t>(a.C) * 2};
+            const uint32_t box[2] = {KD, RAW_ROWS};
+            if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qkv, dim, stride, box))
+                return cudaErrorInvalidValue;
+        }
+        if (a.kda) {  // per-channel gate rows as [B*T][H_v][128], boxes of 16 tokens
+            const uint64_t dim[3] = {KD, static_cast<uint64_t>(a.H_v), static_cast<uint64_t>(a.B) * a.T};
+            const uint64_t stride[2] = {KD * 2, static_cast<uint64_t>(a.H_v) * KD * 2};
+            const uint32_t box[3] = {KD, 1, KC};
+            if (!encode_tiled(&tf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.f, dim, stride, box))
+                return cudaErrorInvalidValue;
+        }
+    }
     const dim3 grid(nchunk, a.H_v, a.B);
     if (a.in_bf16 && a.kda)
-        kda_intra_kernel<true, true><<<grid, 256, 0, stream>>>(a, ws);
+        kda_intra_kernel<true, true><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
     else if (a.in_bf16)
-        kda_intra_kernel<true, false><<<grid, 256, 0, stream>>>(a, ws);
+        kda_intra_kernel<true, false><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
     else if (a.kda)
-        kda_intra_kernel<false, true><<<grid, 256, 0, stream>>>(a, ws);
+        kda_intra_kernel<false, true><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
     else
-        kda_intra_kernel<false, false><<<grid, 256, 0, stream>>>(a, ws);
+        kda_intra_kernel<false, false><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kda_state_kernel<<<dim3(a.H_v, a.B), ST_THREADS, SMEM, stream>>>(a, ws, nchunk, tmz);
