@@ -211,5 +211,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, in
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void *dst_smem, const void *tmap, int x, int y, int z, int w,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(smem_addr(dst_smem)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "r"(smem_addr(bar))
+        : "memory");
+}
+
 }  // namespace dev
 }  // namespace gdn

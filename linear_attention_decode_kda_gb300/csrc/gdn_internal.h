@@ -54,6 +54,7 @@ cudaError_t launch_stream(const StepPlan &plan, const StepArgs &a, bool pdl, cud
 // K % 8 == 0), x fp32 or bf16 rows of stride ldx (16-byte aligned), y fp32 rows
 // of stride ldy.  One launch covers up to kMaxProjSlots slots.
 constexpr int kMaxProjSlots = 4;
+constexpr int kProjTcMinBatch = 16;  // from this batch up the products run on tcgen05 (K % 64 == 0)
 struct ProjSlotDesc {
     const void *w;
     const void *x;
@@ -62,6 +63,7 @@ struct ProjSlotDesc {
 };
 bool proj_slot_ok(const ProjSlotDesc &d);
 cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_t stream);
+unsigned int take_proj_error();
 
 // Read and clear the step kernels' device error words (synchronous).
 unsigned int take_stream_error();

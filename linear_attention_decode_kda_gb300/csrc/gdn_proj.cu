@@ -14,7 +14,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gdn_device.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
+#include "gdn_tmap.h"
 
 namespace gdn {
 namespace {
@@ -33,6 +36,7 @@ struct Slot {
 struct Args {
     Slot s[kMaxProjSlots];
     int nslot, B;
+    int ksplit;  // tensor-core path: K ranges per output tile (partial sums added atomically)
 };
 
 __device__ __forceinline__ void unpack8(const uint4 r, float (&v)[8])
@@ -104,6 +108,233 @@ __global__ void __launch_bounds__(PT) proj_kernel(const __grid_constant__ Args p
     }
 }
 
+// ---------------------------------------------------------------- tcgen05 path
+//
+// From 16 batch rows up the products are dense enough for the tensor core: a
+// CTA takes 128 weight rows (M) against up to 64 batch rows (N), K in tiles of
+// 64 through a ring of 4 shared-memory stages.  Weights are copied into the
+// canonical K-major layout by 16-byte async copies; activations are bf16 (the
+// layer input) or fp32 rows split into bf16 hi + lo, multiplied as W hi + W lo
+// (the weights are exact in bf16).  The fp32 accumulator lives in TMEM.
+
+constexpr int TC_M = 128, TC_N = 64, TC_K = 64, TC_PT = 128;
+constexpr int TC_WB = TC_M * TC_K * 2;   // weight tile bytes
+constexpr int TC_XB = TC_N * TC_K * 2;   // bf16 activation tile (or one half of the split)
+// A weight tile arrives by one TMA box of 64 elements x 128 rows in the 128-byte
+// swizzled K-major layout (tc::op_desc_sw128).  Activation rows arrive as a plain
+// [64][64] box and the threads copy them into the canonical layout (tc::op_offset):
+// bf16 as is, fp32 split into bf16 hi and lo.
+template <bool SPLIT> struct TcCfg {
+    static constexpr int RAW = TC_WB + (SPLIT ? 2 : 1) * TC_XB;  // the activation box
+    static constexpr int RAW_BYTES = TC_N * TC_K * (SPLIT ? 4 : 2);
+    static constexpr int STAGE = RAW + RAW_BYTES;
+    static constexpr int NS = SPLIT ? 4 : 6;  // one CTA an SM
+    static constexpr int LAG = 2;             // refills reuse the stage of the tile 2 back
+    // CTAs to aim for when splitting K (the split's zeroing memsets cost about as much
+    // as a second wave, so a launch that already covers most SMs stays unsplit)
+    static constexpr int TARGET = 160;
+    static constexpr int D = NS - LAG;   // tiles in flight ahead of the product
+    static constexpr int SMEM = NS * STAGE;
+    static constexpr uint32_t TX = TC_WB + RAW_BYTES;
+};
+
+struct TcMaps {
+    CUtensorMap w[kMaxProjSlots], x[kMaxProjSlots];
+};
+
+__device__ unsigned int g_proj_error;
+
+struct TcShared {
+    uint64_t full[8];  // the tile of stage s has arrived
+    uint64_t done[8];  // the products that read stage s have completed
+    uint32_t tmem;
+};
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(TC_PT, 1)
+proj_tc_kernel(const __grid_constant__ Args p, const __grid_constant__ TcMaps maps)
+{
+    using Cfg = TcCfg<SPLIT>;
+    constexpr int NS = Cfg::NS, STAGE = Cfg::STAGE, D = Cfg::D;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ __align__(16) TcShared ts;
+    int si = 0;
+#pragma unroll
+    for (int k = 1; k < kMaxProjSlots; ++k)
+        if (k < p.nslot && static_cast<int>(blockIdx.x) >= p.s[k].cta0) si = k;
+    const Slot &s = p.s[si];
+    const CUtensorMap *mw = &maps.w[si], *mx = &maps.x[si];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int n0 = (static_cast<int>(blockIdx.x) - s.cta0) * TC_M;  // first weight row
+    const int b0 = blockIdx.y * TC_N;                                // first batch row
+    const int nb = min(TC_N, p.B - b0);
+    const int nk = s.K / TC_K / p.ksplit;                           // K tiles of this CTA
+    const int kt0 = blockIdx.z * nk;                                 // its first K tile
+
+    if (warp == 0) tc::tmem_alloc(&ts.tmem, TC_N);
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            dev::mbar_init(&ts.full[i], 1);
+            dev::mbar_init(&ts.done[i], 1);
+        }
+        dev::fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = ts.tmem;
+
+    // tile kt into stage kt % NS (rows past N or past the batch read as zero)
+    auto load = [&](int kt) {
+        unsigned char *st = sm + (kt % NS) * STAGE;
+        dev::mbar_expect_tx(&ts.full[kt % NS], Cfg::TX);
+        dev::tma_load_2d(st, mw, (kt0 + kt) * TC_K, n0, &ts.full[kt % NS]);
+        dev::tma_load_2d(st + Cfg::RAW, mx, (kt0 + kt) * TC_K, b0, &ts.full[kt % NS]);
+    };
+
+    bool ok = true;
+    const uint32_t idesc = tc::idesc_f16(TC_M, TC_N, false, true);
+    if (tid == 0) {
+        dev::prefetch_tensormap(mw);
+        dev::prefetch_tensormap(mx);
+        for (int kt = 0; kt < D && kt < nk; ++kt) load(kt);
+    }
+#pragma unroll 1
+    for (int kt = 0; kt < nk; ++kt) {
+        unsigned char *st = sm + (kt % NS) * STAGE;
+        if (ok) ok = dev::mbar_wait_bounded(&ts.full[kt % NS], static_cast<uint32_t>((kt / NS) & 1));
+        // the activation box -> the canonical layout: fp32 as bf16 hi and lo, bf16 as is
+        if (SPLIT) {
+            const float *xf = reinterpret_cast<const float *>(st + Cfg::RAW);
+#pragma unroll
+            for (int e = 0; e < TC_N * 16 / TC_PT; ++e) {
+                const int pc = tid + e * TC_PT, r = pc >> 4, q = pc & 15;
+                const float4 v = *reinterpret_cast<const float4 *>(xf + r * TC_K + 4 * q);
+                const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+                const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+                const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - f0.x, v.y - f0.y);
+                const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - f1.x, v.w - f1.y);
+                unsigned char *hi = st + TC_WB + tc::op_offset(r, 4 * q, TC_K);
+                uint2 hv, lv;
+                hv.x = *reinterpret_cast<const uint32_t *>(&h0);
+                hv.y = *reinterpret_cast<const uint32_t *>(&h1);
+                lv.x = *reinterpret_cast<const uint32_t *>(&l0);
+                lv.y = *reinterpret_cast<const uint32_t *>(&l1);
+                *reinterpret_cast<uint2 *>(hi) = hv;
+                *reinterpret_cast<uint2 *>(hi + TC_XB) = lv;
+            }
+        } else {
+            const unsigned char *xb = st + Cfg::RAW;
+#pragma unroll
+            for (int e = 0; e < TC_N * 8 / TC_PT; ++e) {
+                const int pc = tid + e * TC_PT, r = pc >> 3, q = pc & 7;
+                *reinterpret_cast<uint4 *>(st + TC_WB + tc::op_offset(r, 8 * q, TC_K)) =
+                    *reinterpret_cast<const uint4 *>(xb + (r * TC_K + 8 * q) * 2);
+            }
+        }
+        dev::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t sa = tc::smem_u32(st);
+#pragma unroll
+            for (int ks = 0; ks < TC_K; ks += 16) {
+                const uint64_t dw = tc::op_desc_sw128(sa, ks);
+                tc::mma_f16(tm, dw, tc::op_desc(sa + TC_WB, ks, TC_K), idesc, kt > 0 || ks > 0);
+                if (SPLIT) tc::mma_f16(tm, dw, tc::op_desc(sa + TC_WB + TC_XB, ks, TC_K), idesc, true);
+            }
+            tc::mma_commit(&ts.done[kt % NS]);
+            // tile kt + D goes where tile kt + D - NS (= kt - LAG) was, once its products are done
+            const int kn = kt + D;
+            if (kn < nk) {
+                if (kn >= NS && ok)
+                    ok = dev::mbar_wait_bounded(&ts.done[kn % NS], static_cast<uint32_t>(((kn - NS) / NS) & 1));
+                load(kn);
+            }
+        }
+    }
+    // the last tile's products, then the accumulator out: lane = weight row
+    if (nk > 0 && ok)
+        ok = dev::mbar_wait_bounded(&ts.done[(nk - 1) % NS], static_cast<uint32_t>(((nk - 1) / NS) & 1));
+    tc::fence_after_sync();
+    const int n = n0 + tid;
+#pragma unroll
+    for (int c0 = 0; c0 < TC_N; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::taddr(tm, 32 * warp, c0), v);
+        if (n < s.N)
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c0 + c < nb) {
+                    float *yp = s.y + static_cast<size_t>(b0 + c0 + c) * s.ldy + n;
+                    if (p.ksplit > 1)
+                        atomicAdd(yp, v[c]);
+                    else
+                        *yp = v[c];
+                }
+    }
+    if (!ok) {
+        // a wait gave up: let every copy and product land (bounded) before the
+        // shared memory and TMEM are released
+        if (tid == 0) {
+            for (int i = 0; i < NS && i < nk; ++i) {
+                const int last = i + NS * ((nk - 1 - i) / NS);
+                dev::mbar_wait_bounded(&ts.full[i], static_cast<uint32_t>((last / NS) & 1));
+                dev::mbar_wait_bounded(&ts.done[i], static_cast<uint32_t>((last / NS) & 1));
+            }
+            atomicOr(&g_proj_error, 1u);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, TC_N);
+}
+
+template <bool SPLIT>
+cudaError_t launch_tc(const Args &a, const ProjSlotDesc *slots, int ctas, int B, cudaStream_t stream)
+{
+    static bool attr_set[64];  // per device; benign race: every writer sets the same value
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(proj_tc_kernel<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcCfg<SPLIT>::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    TcMaps m = {};
+    for (int i = 0; i < a.nslot; ++i) {
+        const ProjSlotDesc &d = slots[i];
+        {   // weights [N][K]: boxes of 64 elements x 128 rows, 128-byte swizzled
+            const uint64_t dim[2] = {static_cast<uint64_t>(d.K), static_cast<uint64_t>(d.N)};
+            const uint64_t stride[1] = {static_cast<uint64_t>(d.K) * 2};
+            const uint32_t box[2] = {TC_K, TC_M};
+            if (!encode_tiled_swizzled(&m.w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d.w, dim, stride, box,
+                                       CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+        }
+        {   // activation rows [B][ldx] as a [B][K] box of 64 rows x 64
+            const uint64_t dim[2] = {static_cast<uint64_t>(d.K), static_cast<uint64_t>(B)};
+            const uint64_t stride[1] = {static_cast<uint64_t>(d.ldx) * (SPLIT ? 4 : 2)};
+            const uint32_t box[2] = {TC_K, TC_N};
+            if (!encode_tiled(&m.x[i], SPLIT ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              2, d.x, dim, stride, box))
+                return cudaErrorInvalidValue;
+        }
+    }
+    if (a.ksplit > 1)  // partial sums are added into zeroed outputs
+        for (int i = 0; i < a.nslot; ++i) {
+            e = cudaMemset2DAsync(slots[i].y, static_cast<size_t>(slots[i].ldy) * sizeof(float), 0,
+                                  static_cast<size_t>(slots[i].N) * sizeof(float), B, stream);
+            if (e != cudaSuccess) return e;
+        }
+    proj_tc_kernel<SPLIT><<<dim3(ctas, (B + TC_N - 1) / TC_N, a.ksplit), TC_PT, TcCfg<SPLIT>::SMEM, stream>>>(a, m);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool proj_slot_ok(const ProjSlotDesc &d)
@@ -122,6 +353,7 @@ cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_
     Args a = {};
     a.nslot = nslot;
     a.B = B;
+    a.ksplit = 1;
     int ctas = 0;
     for (int i = 0; i < nslot; ++i) {
         const ProjSlotDesc &d = slots[i];
@@ -142,6 +374,32 @@ cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_
         const int rows = PT / tpr;
         ctas += (d.N + rows - 1) / rows;
     }
+    // tcgen05 from kProjTcMinBatch batch rows, when every slot's K is a multiple of
+    // 64 and all slots read activations of one type
+    bool tc_ok = B >= kProjTcMinBatch;
+    for (int i = 0; i < nslot; ++i)
+        tc_ok = tc_ok && slots[i].K % TC_K == 0 && slots[i].N % 8 == 0 &&
+                slots[i].x_bf16 == slots[0].x_bf16;
+    if (tc_ok) {
+        int tctas = 0, kmin = 1 << 30;
+        for (int i = 0; i < nslot; ++i) {
+            a.s[i].cta0 = tctas;
+            tctas += (slots[i].N + TC_M - 1) / TC_M;
+            kmin = min(kmin, slots[i].K / TC_K);
+        }
+        // split K until the launch covers the SMs (every slot's K tiles divide evenly)
+        const int ctas_y = tctas * ((B + TC_N - 1) / TC_N);
+        a.ksplit = 1;
+        const int target = slots[0].x_bf16 ? TcCfg<false>::TARGET : TcCfg<true>::TARGET;
+        while (ctas_y * a.ksplit * 2 <= target && a.ksplit * 2 <= kmin) {
+            bool even = true;
+            for (int i = 0; i < nslot; ++i) even = even && (slots[i].K / TC_K) % (a.ksplit * 2) == 0;
+            if (!even) break;
+            a.ksplit *= 2;
+        }
+        return slots[0].x_bf16 ? launch_tc<false>(a, slots, tctas, B, stream)
+                               : launch_tc<true>(a, slots, tctas, B, stream);
+    }
     if (B >= 8)
         proj_kernel<8><<<ctas, PT, 0, stream>>>(a);
     else if (B >= 4)
@@ -151,6 +409,18 @@ cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_
     else
         proj_kernel<1><<<ctas, PT, 0, stream>>>(a);
     return cudaGetLastError();
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+unsigned int take_proj_error()
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_proj_error, sizeof(v)) != cudaSuccess) return ~0u;
+    if (v && cudaMemcpyToSymbol(g_proj_error, &zero, sizeof(zero)) != cudaSuccess) return ~0u;
+    return v;
 }
 
 }  // namespace gdn

@@ -39,6 +39,36 @@ __device__ __forceinline__ uint64_t op_desc(uint32_t base, int k0, int kdim)
     return d;                                               // base offset 0, no swizzle
 }
 
+// Descriptor of a K-major no-swizzle operand laid out with any strides: `lbo`
+// bytes between core matrices adjacent in K, `sbo` bytes between 8-row groups
+// (op_desc is this with lbo = 128 and sbo = kdim * 16).
+__device__ __forceinline__ uint64_t op_desc_strided(uint32_t start, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((start & 0x3FFFF) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Descriptor of a K-major operand in the 128-byte swizzled layout that a TMA box
+// of 64 16-bit elements x R rows with CU_TENSOR_MAP_SWIZZLE_128B writes (1024-byte
+// aligned): rows of 128 bytes, 8-row groups 1024 bytes apart (SBO), the 16-byte
+// chunks of row r permuted by r % 8.  The K step k0 (a multiple of 16 elements,
+// below 64) advances the start address by 2 k0 bytes inside the 128-byte row.
+__device__ __forceinline__ uint64_t op_desc_sw128(uint32_t base, int k0)
+{
+    const uint32_t start = base + static_cast<uint32_t>(k0) * 2;
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((start & 0x3FFFF) >> 4);  // bits 0-13: start address
+    d |= static_cast<uint64_t>(1) << 16;                   // bits 16-29: leading offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // bits 32-45: stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                   // bits 46-48: descriptor version 1
+    d |= static_cast<uint64_t>(2) << 61;                   // bits 61-63: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of kind::f16: fp16 (or bf16) A and B, fp32 D, both K-major.
 __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, bool negate_a, bool bf16 = false)
 {

@@ -27,6 +27,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
 bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
                   const uint64_t *dims, const uint64_t *strides, const uint32_t *box)
 {
+    return encode_tiled_swizzled(map, type, rank, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool encode_tiled_swizzled(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
+                           const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                           CUtensorMapSwizzle swizzle)
+{
     PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
     if (!encode || rank < 1 || rank > 5) return false;
     cuuint64_t d[5], s[4];
@@ -38,7 +45,7 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, int rank, const vo
         if (i + 1 < rank) s[i] = strides[i];
     }
     return encode(map, type, static_cast<cuuint32_t>(rank), const_cast<void *>(base), d, s, b, e,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

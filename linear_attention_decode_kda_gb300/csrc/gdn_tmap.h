@@ -13,5 +13,9 @@ namespace gdn {
 // fill out of bounds).  Returns false if the driver rejects the description.
 bool encode_tiled(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
                   const uint64_t *dims, const uint64_t *strides, const uint32_t *box);
+// The same with a shared-memory swizzle (the box's inner extent at most the swizzle span).
+bool encode_tiled_swizzled(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base,
+                           const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                           CUtensorMapSwizzle swizzle);
 
 }  // namespace gdn
