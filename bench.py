@@ -104,11 +104,32 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
 
 
-def kernel_source_hash() -> str:
+# The sources each workload's kernels are built from: a traffic figure stays valid
+# while these files are unchanged.
+_COMMON_SOURCES = ("gdn_api.cu", "gdn_internal.h", "gdn_device.cuh")
+_STREAM_SOURCES = _COMMON_SOURCES + ("gdn_stream.cu", "gdn_tmap.cu", "gdn_tmap.h")
+_STEP_SOURCES = _COMMON_SOURCES + ("gdn_step.cu",)
+_PREFILL_SOURCES = _COMMON_SOURCES + ("gdn_kda_prefill.cu", "gdn_prefill.cu", "gdn_prefill.h",
+                                      "gdn_tc.cuh", "gdn_tmap.cu", "gdn_tmap.h")
+_LAYER_SOURCES = tuple(sorted(set(_STREAM_SOURCES + _STEP_SOURCES + ("gdn_proj.cu", "gdn_tc.cuh"))))
+
+
+def workload_sources(workload: str):
+    if workload in PREFILL_WORKLOADS:
+        return _PREFILL_SOURCES
+    if workload in LAYER_WORKLOADS:
+        return _LAYER_SOURCES
+    if workload == "kda_decode_b1_34layers":
+        return _STEP_SOURCES
+    return _STREAM_SOURCES
+
+
+def kernel_source_hash(files=None) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_decode_kda_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(files if files is not None else os.listdir(csrc)):
         if fn.endswith((".cu", ".h", ".cuh")):
+            h.update(fn.encode())
             h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
@@ -119,7 +140,7 @@ def ncu_traffic(workload: str):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(workload)
-    if not d or d.get("source_sha256_16") != kernel_source_hash():
+    if not d or d.get("source_sha256_16") != kernel_source_hash(workload_sources(workload)):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -197,6 +218,9 @@ class Workload:
 
     def e2e_step(self, i):
         raise NotImplementedError
+
+    def capture(self, tokens):    # build whatever the timed steps replay (default: nothing)
+        pass
 
     h2d_bytes = 0
     d2h_bytes = 0
@@ -363,9 +387,6 @@ class SingleLaunch(Workload):
         else:
             g.gdn_prefill_chunked(self.abi_shape, self._tensors(j), self.ws.data_ptr(),
                                   self.ws_bytes, st)
-
-    def capture(self, _):
-        pass
 
     def step(self, i):
         self._launch(i % self.n)
