@@ -39,6 +39,18 @@ constexpr int KM1 = 3;  // conv window rows kept between calls (conv_K - 1)
 
 __device__ unsigned int g_step_error;  // bit 0: a bounded mbarrier wait gave up
 
+// Asks L2 to fetch every 128-byte line holding a byte of [p, p + bytes), the lanes
+// of a warp taking alternate lines.  Nothing comes back to the thread, so this may
+// run before the dependency wait on rows the previous kernel is still writing: L2 is
+// the point of coherence, and the loads after the wait read the lines as written.
+__device__ __forceinline__ void prefetch_l2_lines(const void *p, size_t bytes, int lane)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + bytes;
+    for (uintptr_t ad = a0 + 128u * static_cast<uintptr_t>(lane); ad < a1; ad += 32u * 128u)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(ad));
+}
+
 template <int CQ, int CV>
 struct TokenIn {
     float xq[CQ], xk[CQ], fq[CQ], xv[CV];
@@ -137,6 +149,32 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         for (int c = 0; c < 4; ++c) nw[c] = a.norm_w[col0 + c];
     }
     const float dtb_head = a.kda ? 0.0f : a.dt_bias[h];
+
+    // The rows of the first tokens' inputs are asked into L2 now, so that the loads
+    // after the wait find them there (a warp per input segment).
+    {
+        const int ntok = min(a.T, 4);
+        const size_t esz = a.in_bf16 ? 2 : 4;
+        const char *qkv = static_cast<const char *>(a.qkv);
+        for (int s = warp; s < 6 * ntok; s += NWARP) {
+            const size_t bt = static_cast<size_t>(b) * a.T + s / 6;
+            const size_t row = bt * C, bth = bt * a.H_v + h;
+            const void *p = nullptr;
+            size_t n = 0;
+            switch (s % 6) {
+            case 0: p = qkv + (row + hq * D) * esz; n = D; break;
+            case 1: p = qkv + (row + static_cast<size_t>(a.H_qk + hq) * D) * esz; n = D; break;
+            case 2: p = qkv + (row + 2 * static_cast<size_t>(a.H_qk) * D + h * D + slab * W) * esz; n = W; break;
+            case 3:
+                p = static_cast<const char *>(a.f) + (a.kda ? bth * D : bth) * esz;
+                n = a.kda ? D : 1;
+                break;
+            case 4: p = static_cast<const char *>(a.z) + (bth * D + slab * W) * esz; n = W; break;
+            default: p = static_cast<const char *>(a.beta) + bth * esz; n = 1; break;
+            }
+            prefetch_l2_lines(p, n * esz, lane);
+        }
+    }
 
     // ---- inputs may be written by the previous kernel on the stream
     pdl_wait();
