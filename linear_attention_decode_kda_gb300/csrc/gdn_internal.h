@@ -30,7 +30,7 @@ struct StepArgs {
 
 // One launch configuration of the step kernels.
 struct StepPlan {
-    enum Kind { kSlab, kStream } kind = kSlab;
+    enum Kind { kSlab, kStream, kWarp } kind = kSlab;
     int D = 0, W = 0, nslab = 0, threads = 0, cluster = 1, grid = 0;
     const char *name = nullptr;
 };
@@ -41,6 +41,11 @@ cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaS
 // The slab plan for long token loops: as plan_slab, with fewer slabs until the grid is
 // resident at once.
 bool plan_slab_one_wave(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
+
+// Warp-column kernel (gdn_step.cu): d = 128, every reduction of a token inside a
+// warp, 64 or 128 value columns a CTA; planned from 128 (sequence, head) units.
+bool plan_wstep(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
+cudaError_t launch_wstep(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
 
 // Persistent TMA-pipelined kernel (gdn_stream.cu): d = 128, ungrouped heads,
 // at least two (sequence, head) units per SM.
@@ -75,20 +80,24 @@ unsigned int take_step_error();
 inline bool plan_step(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
 {
     return plan_stream(D, B, H_v, group, num_sms, plan) ||
+           plan_wstep(D, B, H_v, group, num_sms, plan) ||
            plan_slab(D, B, H_v, group, num_sms, plan);
 }
 
 // Queues the planned kernel; a streaming plan whose buffers miss the 16-byte
-// chunk rules runs on the column-slab kernel instead.
+// chunk rules runs on the warp-column (d = 128) or column-slab kernel instead.
 inline cudaError_t launch_step(const StepPlan &plan, const StepArgs &a, bool pdl, int num_sms,
                                cudaStream_t stream)
 {
     if (plan.kind == StepPlan::kStream) {
         if (stream_eligible(a)) return launch_stream(plan, a, pdl, stream);
-        StepPlan slab;
-        if (!plan_slab(plan.D, a.B, a.H_v, a.group, num_sms, &slab)) return cudaErrorInvalidValue;
-        return launch_slab(slab, a, pdl, stream);
+        StepPlan other;
+        if (plan_wstep(plan.D, a.B, a.H_v, a.group, num_sms, &other))
+            return launch_wstep(other, a, pdl, stream);
+        if (!plan_slab(plan.D, a.B, a.H_v, a.group, num_sms, &other)) return cudaErrorInvalidValue;
+        return launch_slab(other, a, pdl, stream);
     }
+    if (plan.kind == StepPlan::kWarp) return launch_wstep(plan, a, pdl, stream);
     return launch_slab(plan, a, pdl, stream);
 }
 

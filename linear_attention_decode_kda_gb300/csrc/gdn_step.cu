@@ -443,6 +443,340 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     }
 }
 
+// ---------------------------------------------------------------- warp-column form (d = 128)
+//
+// The same step at d = 128 with every reduction of a token inside one warp: a warp
+// owns 8 value columns of the head and all 128 key rows (lane l: rows 4l..4l+3, so
+// 32 state values a lane), and computes the conv, the norms and the decay of the
+// head's q/k channels for its own rows.  The column sums S_t^T k and S_t^T q of its
+// 8 columns are a 16-value reduce-scatter over the warp (16 shuffles), after which
+// lanes 2c and 2c+1 hold column c's k-sum (lanes 0..15) or q-sum (lanes 16..31).
+// Nothing but the RMS norm's sum over the head's 128 columns leaves the warp:
+// through shared memory when one CTA holds the head, else by st.async pushes to
+// every CTA of the head inside a cluster, as in the slab form above.
+// Scalar maps use the hardware exponential, logarithm and reciprocal.
+
+constexpr int WD = 128;   // key and value width of this form
+constexpr int WCOL = 8;   // value columns per warp
+
+__device__ __forceinline__ float fast_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float fast_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float fast_softplus(float x)
+{
+    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
+}
+
+struct WIn {
+    float q[4], k[4], f[4];
+    float vz;  // lanes 0..15: v of column (lane/2)%8; lanes 16..31: z of that column
+    float beta, fh;
+};
+
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
+{
+    constexpr int D = WD;
+    constexpr int W = WCOL * NW;     // value columns of the CTA
+    constexpr int NSLAB = D / W;     // CTAs per head
+    constexpr unsigned FULL = 0xffffffffu;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hq = h / a.group;
+    const bool clustered = NSLAB * a.group > 1;
+    const bool qk_owner = slab == 0 && h % a.group == 0 && warp == 0;  // writes the q/k window
+    const int C = a.C;
+    const int r0 = 4 * lane;                 // key rows (channels) of this lane
+    const int jc = (lane >> 1) & 7;          // the column whose sums this lane holds
+    const bool klane = lane < 16;            // k-sum (and v) lanes; the others q-sum (and z)
+    const bool vown = klane && (lane & 1) == 0;  // reads and writes column jc's v window
+    const int c0 = slab * W + WCOL * warp;   // first value column of the warp
+
+    __shared__ float4 cw_s[2][4][32];        // conv taps of the head's q and k channels, [i][lane]
+    __shared__ float rms_slot[2][NSLAB * NW];  // the warps' sums of o^2, by token parity
+    __shared__ __align__(8) uint64_t rms_bar[2];
+
+    pdl_launch_dependents();
+    uint32_t rank0 = 0;  // cluster rank of slab 0 of this head
+    if (NSLAB > 1 || clustered) {
+        rank0 = cluster_rank() - slab;
+        if (NSLAB > 1 && tid == 0) {
+            mbar_init(&rms_bar[0], 1);
+            mbar_init(&rms_bar[1], 1);
+            fence_mbar_init();
+        }
+    }
+    bool ok = true;
+
+    // ---- before the dependency wait: state, conv windows and taps, parameters
+    const size_t head = static_cast<size_t>(b) * a.H_v + h;
+    float st[4][WCOL];
+    {
+        const float *S = a.state_in + head * D * D + c0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 lo = *reinterpret_cast<const float4 *>(S + static_cast<size_t>(r0 + i) * D);
+            const float4 hi = *reinterpret_cast<const float4 *>(S + static_cast<size_t>(r0 + i) * D + 4);
+            st[i][0] = lo.x; st[i][1] = lo.y; st[i][2] = lo.z; st[i][3] = lo.w;
+            st[i][4] = hi.x; st[i][5] = hi.y; st[i][6] = hi.z; st[i][7] = hi.w;
+        }
+    }
+    const int cq = hq * D + r0, ck = (a.H_qk + hq) * D + r0;
+    const int cv = 2 * a.H_qk * D + h * D + c0 + jc;
+    float wq[4][KM1], wk[4][KM1], wv[KM1] = {0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < KM1; ++r) {
+        const float *row = a.conv_in + (static_cast<size_t>(b) * KM1 + r) * C;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            wq[i][r] = row[cq + i];
+            wk[i][r] = row[ck + i];
+        }
+        if (vown) wv[r] = row[cv];
+    }
+    for (int e = tid; e < 2 * 4 * 32; e += NW * 32) {
+        const int s = e >> 7, i = (e >> 5) & 3, l = e & 31;
+        cw_s[s][i][l] = reinterpret_cast<const float4 *>(a.conv_w)[(s ? a.H_qk + hq : hq) * D + 4 * l + i];
+    }
+    const float4 cwv = vown ? reinterpret_cast<const float4 *>(a.conv_w)[cv] : make_float4(0.f, 0.f, 0.f, 0.f);
+    // softplus gates: A = exp(A_log); lower-bound gate: A = the scale a, lbv = the bound
+    const float A = a.lb_gate ? a.A_log[h] : __expf(a.A_log[h]);
+    const float lbv = a.lb_gate ? a.dt_bias[h] : 0.0f;
+    float dtb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dtb[i] = a.kda && !a.lb_gate ? a.dt_bias[static_cast<size_t>(h) * D + r0 + i] : 0.0f;
+    const float dtb_head = a.kda ? 0.0f : a.dt_bias[h];
+    const float nw = klane ? 0.0f : a.norm_w[c0 + jc];
+
+    // The first tokens' input rows are asked into L2 before the wait (a warp per segment).
+    {
+        const int ntok = min(a.T, 4);
+        const size_t esz = a.in_bf16 ? 2 : 4;
+        const char *qkv = static_cast<const char *>(a.qkv);
+        for (int s = warp; s < 6 * ntok; s += NW) {
+            const size_t bt = static_cast<size_t>(b) * a.T + s / 6;
+            const size_t row = bt * C, bth = bt * a.H_v + h;
+            const void *p = nullptr;
+            size_t n = 0;
+            switch (s % 6) {
+            case 0: p = qkv + (row + hq * D) * esz; n = D; break;
+            case 1: p = qkv + (row + static_cast<size_t>(a.H_qk + hq) * D) * esz; n = D; break;
+            case 2: p = qkv + (row + 2 * static_cast<size_t>(a.H_qk) * D + h * D + slab * W) * esz; n = W; break;
+            case 3:
+                p = static_cast<const char *>(a.f) + (a.kda ? bth * D : bth) * esz;
+                n = a.kda ? D : 1;
+                break;
+            case 4: p = static_cast<const char *>(a.z) + (bth * D + slab * W) * esz; n = W; break;
+            default: p = static_cast<const char *>(a.beta) + bth * esz; n = 1; break;
+            }
+            prefetch_l2_lines(p, n * esz, lane);
+        }
+    }
+    // Every read of the conv window (and the barrier set-up) is ordered before the
+    // window's in-place update by the writing warp, which passes this barrier's wait
+    // before its first token.
+    if (NSLAB > 1 || clustered) cluster_arrive_release();
+    __syncthreads();  // conv taps in shared memory; the CTA's own window reads
+
+    // ---- inputs may be written by the previous kernel on the stream
+    pdl_wait();
+
+    auto load_token = [&](int t, WIn &in) {
+        const size_t bt = static_cast<size_t>(b) * a.T + t;
+        const size_t row = bt * C, bth = bt * a.H_v + h;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            in.q[i] = ld_in(a.qkv, row + cq + i, a.in_bf16);
+            in.k[i] = ld_in(a.qkv, row + ck + i, a.in_bf16);
+            in.f[i] = a.kda ? ld_in(a.f, bth * D + r0 + i, a.in_bf16) : 0.0f;
+        }
+        in.vz = klane ? ld_in(a.qkv, row + cv, a.in_bf16) : ld_in(a.z, bth * D + c0 + jc, a.in_bf16);
+        in.beta = ld_in(a.beta, bth, a.in_bf16);
+        in.fh = a.kda ? 0.0f : ld_in(a.f, bth, a.in_bf16);
+    };
+
+    WIn cur;
+    const int Tb = a.accepted ? min(max(a.accepted[b], 0), a.T) : a.T;
+    if (Tb > 0) load_token(0, cur);
+    if (NSLAB > 1 || clustered) cluster_wait_acquire();  // every CTA's barriers and window reads
+
+#pragma unroll 1
+    for (int t = 0; t < Tb; ++t) {
+        WIn nxt;
+        if (t + 1 < Tb) load_token(t + 1, nxt);
+        const size_t bth = (static_cast<size_t>(b) * a.T + t) * a.H_v + h;
+
+        // 1. conv + SiLU of the lane's q/k channels, their decay, v of column jc, beta
+        float q[4], k[4], al[4];
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+        const float alh = a.kda ? 0.0f : __expf(-A * fast_softplus(cur.fh + dtb_head));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 tq = cw_s[0][i][lane], tk = cw_s[1][i][lane];
+            float xq = tq.x * wq[i][0];
+            xq = fmaf(tq.y, wq[i][1], xq);
+            xq = fmaf(tq.z, wq[i][2], xq);
+            xq = fmaf(tq.w, cur.q[i], xq);
+            float xk = tk.x * wk[i][0];
+            xk = fmaf(tk.y, wk[i][1], xk);
+            xk = fmaf(tk.z, wk[i][2], xk);
+            xk = fmaf(tk.w, cur.k[i], xk);
+            q[i] = fast_silu(xq);
+            k[i] = fast_silu(xk);
+            wq[i][0] = wq[i][1]; wq[i][1] = wq[i][2]; wq[i][2] = cur.q[i];
+            wk[i][0] = wk[i][1]; wk[i][1] = wk[i][2]; wk[i][2] = cur.k[i];
+            sq = fmaf(q[i], q[i], sq);
+            sk = fmaf(k[i], k[i], sk);
+            sqk = fmaf(q[i], k[i], sqk);
+            al[i] = !a.kda ? alh
+                  : a.lb_gate ? __expf(lbv * fast_sigmoid(-A * cur.f[i]))
+                              : __expf(-A * fast_softplus(cur.f[i] + dtb[i]));
+        }
+        float vv = 0.f;
+        if (vown) {
+            float x = cwv.x * wv[0];
+            x = fmaf(cwv.y, wv[1], x);
+            x = fmaf(cwv.z, wv[2], x);
+            x = fmaf(cwv.w, cur.vz, x);
+            vv = fast_silu(x);
+            wv[0] = wv[1]; wv[1] = wv[2]; wv[2] = cur.vz;
+        }
+        vv = __shfl_sync(FULL, vv, lane & ~1);
+        const float beta = fast_sigmoid(cur.beta);
+        const bool last = (t == Tb - 1);
+        // the window after the last token (commit): every reader has passed the barrier above
+        if (last && a.conv_out) {
+            float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
+#pragma unroll
+            for (int r = 0; r < KM1; ++r) {
+                if (qk_owner) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        co[static_cast<size_t>(r) * C + cq + i] = wq[i][r];
+                        co[static_cast<size_t>(r) * C + ck + i] = wk[i][r];
+                    }
+                }
+                if (vown) co[static_cast<size_t>(r) * C + cv] = wv[r];
+            }
+        }
+
+        // 2. decay, and the lane's parts of S_t^T k and S_t^T q (raw q, k; scaled below)
+        float red[2 * WCOL];
+#pragma unroll
+        for (int c = 0; c < 2 * WCOL; ++c) red[c] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int c = 0; c < WCOL; ++c) {
+                st[i][c] *= al[i];
+                red[c] = fmaf(st[i][c], k[i], red[c]);
+                red[WCOL + c] = fmaf(st[i][c], q[i], red[WCOL + c]);
+            }
+        }
+        // the norms' sums over the head's 128 channels (all lanes)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sq += __shfl_xor_sync(FULL, sq, off);
+            sk += __shfl_xor_sync(FULL, sk, off);
+            sqk += __shfl_xor_sync(FULL, sqk, off);
+        }
+        // reduce-scatter: after the rounds lane l holds value (l >> 1) summed over the warp
+#pragma unroll
+        for (int n = WCOL; n >= 1; n >>= 1) {
+            const int off = 2 * n;  // 16, 8, 4, 2
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+                const float send = up ? red[i] : red[i + n];
+                const float keep = up ? red[i + n] : red[i];
+                red[i] = keep + __shfl_xor_sync(FULL, send, off);
+            }
+        }
+        const float tot = red[0] + __shfl_xor_sync(FULL, red[0], 1);
+        const float rq = a.q_scale * rsqrtf(sq + a.eps_l2);
+        const float rk = rsqrtf(sk + a.eps_l2);
+        const float kq = sqk * rq * rk;
+
+        // 3. u (k lanes) and o (q lanes) of column jc
+        const float u = beta * (vv - rk * tot);
+        const float o = fmaf(kq, __shfl_xor_sync(FULL, u, 16), rq * tot);
+
+        // 4. state update, stores (they do not wait for the RMS exchange)
+        float *hist = a.state_hist
+            ? a.state_hist + ((static_cast<size_t>(t) * a.B + b) * a.H_v + h) * D * D + c0
+            : nullptr;
+        float *commit = (a.state_out && last) ? a.state_out + head * D * D + c0 : nullptr;
+        float ub[WCOL];
+#pragma unroll
+        for (int c = 0; c < WCOL; ++c) ub[c] = __shfl_sync(FULL, u, 2 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float kn = k[i] * rk;
+#pragma unroll
+            for (int c = 0; c < WCOL; ++c) st[i][c] = fmaf(kn, ub[c], st[i][c]);
+            const size_t off = static_cast<size_t>(r0 + i) * D;
+            const float4 lo = make_float4(st[i][0], st[i][1], st[i][2], st[i][3]);
+            const float4 hi = make_float4(st[i][4], st[i][5], st[i][6], st[i][7]);
+            if (hist) {
+                __stcs(reinterpret_cast<float4 *>(hist + off), lo);
+                __stcs(reinterpret_cast<float4 *>(hist + off + 4), hi);
+            }
+            if (commit) {
+                __stcs(reinterpret_cast<float4 *>(commit + off), lo);
+                __stcs(reinterpret_cast<float4 *>(commit + off + 4), hi);
+            }
+        }
+
+        // 5. gated RMSNorm over the head's 128 columns
+        float p = (!klane && (lane & 1) == 0) ? o * o : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(FULL, p, off);
+        float total = 0.f;
+        const int par = t & 1;
+        if (NSLAB == 1) {
+            if (lane == 0) rms_slot[par][warp] = p;
+            __syncthreads();
+        } else {
+            // each warp's sum to its slot in every CTA of the head
+            if (tid == 0) mbar_expect_tx(&rms_bar[par], NSLAB * NW * 4);
+            if (lane < NSLAB)
+                st_async_remote(&rms_slot[par][slab * NW + warp], rank0 + lane, p, &rms_bar[par]);
+            ok &= mbar_wait_cluster_bounded(&rms_bar[par], static_cast<uint32_t>(t >> 1) & 1u);
+        }
+#pragma unroll
+        for (int s = 0; s < NSLAB * NW; ++s) total += rms_slot[par][s];
+        if (!klane && (lane & 1) == 0 && a.out) {
+            const float rinv = rsqrtf(total * (1.0f / D) + a.eps_norm);
+            const float g = a.sig_gate ? fast_sigmoid(cur.vz) : fast_silu(cur.vz);
+            const float y = o * rinv * nw * g;
+            const size_t idx = bth * D + c0 + jc;
+            if (a.out_bf16)
+                reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
+            else
+                reinterpret_cast<float *>(a.out)[idx] = y;
+        }
+
+        // conv window after this token (verify history)
+        if (a.conv_hist) {
+            float *ch = a.conv_hist + (static_cast<size_t>(t) * a.B + b) * KM1 * C;
+#pragma unroll
+            for (int r = 0; r < KM1; ++r) {
+                if (qk_owner) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        ch[static_cast<size_t>(r) * C + cq + i] = wq[i][r];
+                        ch[static_cast<size_t>(r) * C + ck + i] = wk[i][r];
+                    }
+                }
+                if (vown) ch[static_cast<size_t>(r) * C + cv] = wv[r];
+            }
+        }
+        cur = nxt;
+    }
+
+    if (!ok) atomicOr(&g_step_error, 1u);
+}
+
 struct Variant {
     int D, W, NT;
     void (*fn)(StepArgs);
@@ -525,6 +859,78 @@ cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaS
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.nslab, a.H_v, a.B);
     cfg.blockDim = dim3(plan.threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (plan.cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = plan.nslab;
+        attr[n].val.clusterDim.y = a.group;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, v->fn, a);
+}
+
+namespace {
+
+struct WVariant {
+    int NW;
+    void (*fn)(StepArgs);
+    const char *name;
+};
+const WVariant kWVariants[] = {
+    {8, wstep_kernel<8>, "wstep<128,64>"},
+    {16, wstep_kernel<16>, "wstep<128,128>"},
+};
+
+const WVariant *find_wvariant(int W)
+{
+    for (const WVariant &v : kWVariants)
+        if (WCOL * v.NW == W) return &v;
+    return nullptr;
+}
+
+}  // namespace
+
+bool plan_wstep(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
+{
+    (void)num_sms;
+    if (D != WD || group < 1 || group > 8) return false;
+    const long units = static_cast<long>(B) * H_v;
+    // Below 128 units the column-slab kernel, whose 8-way slabs spread a head's state
+    // over more SMs, keeps the shorter chain (B1 H32: 5.2 against 5.3 us a launch; B2:
+    // 6.0 against 6.7).  From 128 units two 64-column slabs a head measured fastest
+    // (B4 H32: 8.4 us, against 11.1 on the slab kernel and 9.0 with whole heads).
+    if (units < 128) return false;
+    const int best = 2 * group <= 8 ? 2 : 1;
+    const WVariant *v = find_wvariant(D / best);
+    plan->kind = StepPlan::kWarp;
+    plan->D = D;
+    plan->W = D / best;
+    plan->nslab = best;
+    plan->threads = v->NW * 32;
+    plan->cluster = best * group;
+    plan->grid = static_cast<int>(units) * best;
+    plan->name = v->name;
+    return true;
+}
+
+cudaError_t launch_wstep(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
+{
+    const WVariant *v = find_wvariant(plan.W);
+    if (!v || plan.D != WD) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.nslab, a.H_v, a.B);
+    cfg.blockDim = dim3(v->NW * 32, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];

@@ -179,7 +179,7 @@ def test_variant_choice(lib):
     # B*H_v head units: enough for two CTAs per SM -> streaming CTAs; B=1 -> 16-column slabs
     assert gdn.gdn_kernel_variant(_shape(B=64, H_qk=32, H_v=32), gdn.OP_DECODE) == "stream<128>"
     assert gdn.gdn_kernel_variant(_shape(B=32, H_qk=32, H_v=32), gdn.OP_VERIFY) == "stream<128>"
-    assert gdn.gdn_kernel_variant(_shape(B=64, H_qk=16, H_v=32), gdn.OP_DECODE) == "step<128,128>"
+    assert gdn.gdn_kernel_variant(_shape(B=64, H_qk=16, H_v=32), gdn.OP_DECODE) == "wstep<128,64>"
     assert gdn.gdn_kernel_variant(_shape(B=1, H_qk=32, H_v=32), gdn.OP_DECODE) == "step<128,16>"
     assert gdn.gdn_kernel_variant(_shape(d_k=16, d_v=16), gdn.OP_DECODE) == "step<16,16>"
     assert gdn.gdn_kernel_variant(_shape(d_k=48, d_v=48), gdn.OP_DECODE) is None
