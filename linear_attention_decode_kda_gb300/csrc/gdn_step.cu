@@ -22,11 +22,14 @@
 //   2. St = Diag(alpha) S in registers with both column reductions St^T k and
 //      St^T q in one pass (warp shuffles, then one shared-memory round);
 //   3. u = beta (v - St^T k); o = St^T q + (k.q) u  (= S_new^T q);
-//   4. gated RMSNorm over the head's D columns (cluster exchange happens
-//      before any global store, so its release fence has nothing to drain);
-//   5. S_new = St + k u^T stored with 128-bit streaming stores.
-// The state stays in registers across the T tokens of a verify, so verify and
-// T decode calls run the same arithmetic per token.
+//   4. S_new = St + k u^T stored with 128-bit streaming stores, which do not
+//      wait for the norm;
+//   5. gated RMSNorm over the head's D columns (one partial sum per slab,
+//      exchanged inside the cluster).
+// The final conv window is written right after the last token's conv, behind a
+// cluster barrier that every CTA passes once its window reads are done.  The
+// state stays in registers across the T tokens of a verify, so verify and T
+// decode calls run the same arithmetic per token.
 #include "gdn_device.cuh"
 #include "gdn_internal.h"
 
@@ -38,6 +41,25 @@ using namespace dev;
 constexpr int KM1 = 3;  // conv window rows kept between calls (conv_K - 1)
 
 __device__ unsigned int g_step_error;  // bit 0: a bounded mbarrier wait gave up
+
+// The step's scalar maps on the hardware exponential, logarithm and reciprocal
+// (about 2 ulp each in fp32, far inside the step's error budget).
+__device__ __forceinline__ float fast_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float fast_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float fast_softplus(float x)
+{
+    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
+}
+
+// 4-tap causal conv + SiLU: taps 0..2 on the kept window (oldest first), tap 3 on x.
+__device__ __forceinline__ float conv4_fast_silu(const float4 w, const float *win, float x)
+{
+    float acc = w.x * win[0];
+    acc = fmaf(w.y, win[1], acc);
+    acc = fmaf(w.z, win[2], acc);
+    acc = fmaf(w.w, x, acc);
+    return fast_silu(acc);
+}
 
 // Asks L2 to fetch every 128-byte line holding a byte of [p, p + bytes), the lanes
 // of a warp taking alternate lines.  Nothing comes back to the thread, so this may
@@ -96,7 +118,6 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             mbar_init(&rms_bar[1], 1);
             fence_mbar_init();
         }
-        cluster_arrive_relaxed();
     }
 
     bool ok = true;  // false once a bounded wait gave up
@@ -115,7 +136,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     float4 cwq[CQ], cwk[CQ], cwv[CV];
     float dtb[CQ];
     // softplus gates: A = exp(A_log); lower-bound gate: A = the scale a, lbv = the bound
-    const float A = a.lb_gate ? a.A_log[h] : expf(a.A_log[h]);
+    const float A = a.lb_gate ? a.A_log[h] : __expf(a.A_log[h]);
     const float lbv = a.lb_gate ? a.dt_bias[h] : 0.0f;
 #pragma unroll
     for (int m = 0; m < CQ; ++m) {
@@ -176,6 +197,11 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         }
     }
 
+    // Every CTA's reads of the conv window (and its barrier set-up) are ordered before
+    // the window's in-place update, which the writing threads make after this barrier's
+    // wait.  Within a CTA each window channel is read and written by the same thread.
+    if (clustered) cluster_arrive_release();
+
     // ---- inputs may be written by the previous kernel on the stream
     pdl_wait();
 
@@ -212,7 +238,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     // tokens taken for this sequence: all T, or the caller's accepted count
     const int Tb = a.accepted ? min(max(a.accepted[b], 0), a.T) : a.T;
     if (Tb > 0) load_token(0, cur);
-    if (clustered) cluster_wait_acquire();  // every CTA of the cluster has set up its barriers
+    if (clustered) cluster_wait_acquire();  // every CTA's barriers and window reads
 
 #pragma unroll 1
     for (int t = 0; t < Tb; ++t) {
@@ -227,8 +253,8 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         for (int m = 0; m < CQ; ++m) {
             const int i = tid + m * NT;
             if (i < D) {
-                const float q = conv4_silu(cwq[m], wq[m], cur.xq[m]);
-                const float k = conv4_silu(cwk[m], wk[m], cur.xk[m]);
+                const float q = conv4_fast_silu(cwq[m], wq[m], cur.xq[m]);
+                const float k = conv4_fast_silu(cwk[m], wk[m], cur.xk[m]);
                 wq[m][0] = wq[m][1]; wq[m][1] = wq[m][2]; wq[m][2] = cur.xq[m];
                 wk[m][0] = wk[m][1]; wk[m][1] = wk[m][2]; wk[m][2] = cur.xk[m];
                 q_s[i] = q;
@@ -237,21 +263,46 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
                 sk = fmaf(k, k, sk);
                 sqk = fmaf(q, k, sqk);
                 if (a.kda)
-                    a_s[i] = a.lb_gate ? expf(lbv * sigmoid_f(-A * cur.fq[m]))
-                                       : expf(-A * softplus_f(cur.fq[m] + dtb[m]));
+                    a_s[i] = a.lb_gate ? __expf(lbv * fast_sigmoid(-A * cur.fq[m]))
+                                       : __expf(-A * fast_softplus(cur.fq[m] + dtb[m]));
             }
         }
 #pragma unroll
         for (int m = 0; m < CV; ++m) {
             const int j = tv + m * NT;
             if (j < W) {
-                v_s[j] = conv4_silu(cwv[m], wv[m], cur.xv[m]);
+                v_s[j] = conv4_fast_silu(cwv[m], wv[m], cur.xv[m]);
                 wv[m][0] = wv[m][1]; wv[m][1] = wv[m][2]; wv[m][2] = cur.xv[m];
             }
         }
         if (tid == 0) {
-            if (!a.kda) a_s[0] = expf(-A * softplus_f(cur.fh + dtb_head));
-            beta_s = sigmoid_f(cur.beta);
+            if (!a.kda) a_s[0] = __expf(-A * fast_softplus(cur.fh + dtb_head));
+            beta_s = fast_sigmoid(cur.beta);
+        }
+        // the window after the last token (commit): every reader has passed the barrier above
+        if (a.conv_out && t == Tb - 1) {
+            float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
+#pragma unroll
+            for (int m = 0; m < CQ; ++m) {
+                const int i = tid + m * NT;
+                if (i < D && qk_owner) {
+                    const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
+#pragma unroll
+                    for (int r = 0; r < KM1; ++r) {
+                        co[static_cast<size_t>(r) * C + cq] = wq[m][r];
+                        co[static_cast<size_t>(r) * C + ck] = wk[m][r];
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < CV; ++m) {
+                const int j = tv + m * NT;
+                if (j < W) {
+                    const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
+#pragma unroll
+                    for (int r = 0; r < KM1; ++r) co[static_cast<size_t>(r) * C + cv] = wv[m][r];
+                }
+            }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -273,8 +324,8 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             Sk += red3[w][1];
             Sqk += red3[w][2];
         }
-        const float rq = a.q_scale / sqrtf(Sq + a.eps_l2);
-        const float rk = 1.0f / sqrtf(Sk + a.eps_l2);
+        const float rq = a.q_scale * rsqrtf(Sq + a.eps_l2);
+        const float rk = rsqrtf(Sk + a.eps_l2);
         const float kq = Sqk * rq * rk;
         const float beta = beta_s;
 
@@ -368,11 +419,11 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             }
         }
         if (rg == 0 && a.out) {
-            const float rinv = 1.0f / sqrtf(total / static_cast<float>(D) + a.eps_norm);
+            const float rinv = rsqrtf(total * (1.0f / D) + a.eps_norm);
             float y[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                y[c] = o[c] * rinv * nw[c] * (a.sig_gate ? sigmoid_f(cur.z[c]) : silu_f(cur.z[c]));
+                y[c] = o[c] * rinv * nw[c] * (a.sig_gate ? fast_sigmoid(cur.z[c]) : fast_silu(cur.z[c]));
             store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
         }
 
@@ -404,43 +455,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         cur = nxt;
     }
 
-    // final conv window (commit), after every reader of the shared q/k rows:
-    // grouped heads pass a cluster barrier; the slabs of one head have each
-    // pushed partial sums computed from their window reads, all of which this
-    // CTA's waiting threads have received
-    if (clustered) {
-        if (a.group > 1) {
-            cluster_arrive_release();
-            cluster_wait_acquire();
-        } else {
-            __syncthreads();
-        }
-    }
     if (!ok) atomicOr(&g_step_error, 1u);
-    if (a.conv_out && Tb > 0) {
-        float *co = a.conv_out + static_cast<size_t>(b) * KM1 * C;
-#pragma unroll
-        for (int m = 0; m < CQ; ++m) {
-            const int i = tid + m * NT;
-            if (i < D && qk_owner) {
-                const int cq = hq * D + i, ck = a.H_qk * D + hq * D + i;
-#pragma unroll
-                for (int r = 0; r < KM1; ++r) {
-                    co[static_cast<size_t>(r) * C + cq] = wq[m][r];
-                    co[static_cast<size_t>(r) * C + ck] = wk[m][r];
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < CV; ++m) {
-            const int j = tv + m * NT;
-            if (j < W) {
-                const int cv = 2 * a.H_qk * D + h * D + slab * W + j;
-#pragma unroll
-                for (int r = 0; r < KM1; ++r) co[static_cast<size_t>(r) * C + cv] = wv[m][r];
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------- warp-column form (d = 128)
@@ -459,12 +474,6 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
 constexpr int WD = 128;   // key and value width of this form
 constexpr int WCOL = 8;   // value columns per warp
 
-__device__ __forceinline__ float fast_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float fast_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float fast_softplus(float x)
-{
-    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
-}
 
 struct WIn {
     float q[4], k[4], f[4];
