@@ -33,6 +33,23 @@ __device__ __forceinline__ float conv4_silu(const float4 w, const float *win, fl
     return silu_f(acc);
 }
 
+// The same maps on the hardware exponential, logarithm and reciprocal (about 2 ulp
+// each in fp32, far inside the step's error budget); the step kernels use these.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float softplus_fast(float x)
+{
+    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
+}
+__device__ __forceinline__ float conv4_silu_fast(const float4 w, const float *win, float x)
+{
+    float acc = w.x * win[0];
+    acc = fmaf(w.y, win[1], acc);
+    acc = fmaf(w.z, win[2], acc);
+    acc = fmaf(w.w, x, acc);
+    return silu_fast(acc);
+}
+
 __device__ __forceinline__ void store_out4(void *out, size_t idx, int bf16, float a, float b,
                                            float c, float d)
 {

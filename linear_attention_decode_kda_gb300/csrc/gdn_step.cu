@@ -42,25 +42,6 @@ constexpr int KM1 = 3;  // conv window rows kept between calls (conv_K - 1)
 
 __device__ unsigned int g_step_error;  // bit 0: a bounded mbarrier wait gave up
 
-// The step's scalar maps on the hardware exponential, logarithm and reciprocal
-// (about 2 ulp each in fp32, far inside the step's error budget).
-__device__ __forceinline__ float fast_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float fast_silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float fast_softplus(float x)
-{
-    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
-}
-
-// 4-tap causal conv + SiLU: taps 0..2 on the kept window (oldest first), tap 3 on x.
-__device__ __forceinline__ float conv4_fast_silu(const float4 w, const float *win, float x)
-{
-    float acc = w.x * win[0];
-    acc = fmaf(w.y, win[1], acc);
-    acc = fmaf(w.z, win[2], acc);
-    acc = fmaf(w.w, x, acc);
-    return fast_silu(acc);
-}
-
 // Asks L2 to fetch every 128-byte line holding a byte of [p, p + bytes), the lanes
 // of a warp taking alternate lines.  Nothing comes back to the thread, so this may
 // run before the dependency wait on rows the previous kernel is still writing: L2 is
@@ -72,6 +53,7 @@ __device__ __forceinline__ void prefetch_l2_lines(const void *p, size_t bytes, i
     for (uintptr_t ad = a0 + 128u * static_cast<uintptr_t>(lane); ad < a1; ad += 32u * 128u)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(ad));
 }
+
 
 template <int CQ, int CV>
 struct TokenIn {
@@ -253,8 +235,8 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         for (int m = 0; m < CQ; ++m) {
             const int i = tid + m * NT;
             if (i < D) {
-                const float q = conv4_fast_silu(cwq[m], wq[m], cur.xq[m]);
-                const float k = conv4_fast_silu(cwk[m], wk[m], cur.xk[m]);
+                const float q = conv4_silu_fast(cwq[m], wq[m], cur.xq[m]);
+                const float k = conv4_silu_fast(cwk[m], wk[m], cur.xk[m]);
                 wq[m][0] = wq[m][1]; wq[m][1] = wq[m][2]; wq[m][2] = cur.xq[m];
                 wk[m][0] = wk[m][1]; wk[m][1] = wk[m][2]; wk[m][2] = cur.xk[m];
                 q_s[i] = q;
@@ -263,21 +245,21 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
                 sk = fmaf(k, k, sk);
                 sqk = fmaf(q, k, sqk);
                 if (a.kda)
-                    a_s[i] = a.lb_gate ? __expf(lbv * fast_sigmoid(-A * cur.fq[m]))
-                                       : __expf(-A * fast_softplus(cur.fq[m] + dtb[m]));
+                    a_s[i] = a.lb_gate ? __expf(lbv * sigmoid_fast(-A * cur.fq[m]))
+                                       : __expf(-A * softplus_fast(cur.fq[m] + dtb[m]));
             }
         }
 #pragma unroll
         for (int m = 0; m < CV; ++m) {
             const int j = tv + m * NT;
             if (j < W) {
-                v_s[j] = conv4_fast_silu(cwv[m], wv[m], cur.xv[m]);
+                v_s[j] = conv4_silu_fast(cwv[m], wv[m], cur.xv[m]);
                 wv[m][0] = wv[m][1]; wv[m][1] = wv[m][2]; wv[m][2] = cur.xv[m];
             }
         }
         if (tid == 0) {
-            if (!a.kda) a_s[0] = __expf(-A * fast_softplus(cur.fh + dtb_head));
-            beta_s = fast_sigmoid(cur.beta);
+            if (!a.kda) a_s[0] = __expf(-A * softplus_fast(cur.fh + dtb_head));
+            beta_s = sigmoid_fast(cur.beta);
         }
         // the window after the last token (commit): every reader has passed the barrier above
         if (a.conv_out && t == Tb - 1) {
@@ -423,7 +405,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             float y[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                y[c] = o[c] * rinv * nw[c] * (a.sig_gate ? fast_sigmoid(cur.z[c]) : fast_silu(cur.z[c]));
+                y[c] = o[c] * rinv * nw[c] * (a.sig_gate ? sigmoid_fast(cur.z[c]) : silu_fast(cur.z[c]));
             store_out4(a.out, bth * D + col0, a.out_bf16, y[0], y[1], y[2], y[3]);
         }
 
@@ -618,7 +600,7 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
         // 1. conv + SiLU of the lane's q/k channels, their decay, v of column jc, beta
         float q[4], k[4], al[4];
         float sq = 0.f, sk = 0.f, sqk = 0.f;
-        const float alh = a.kda ? 0.0f : __expf(-A * fast_softplus(cur.fh + dtb_head));
+        const float alh = a.kda ? 0.0f : __expf(-A * softplus_fast(cur.fh + dtb_head));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float4 tq = cw_s[0][i][lane], tk = cw_s[1][i][lane];
@@ -630,16 +612,16 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
             xk = fmaf(tk.y, wk[i][1], xk);
             xk = fmaf(tk.z, wk[i][2], xk);
             xk = fmaf(tk.w, cur.k[i], xk);
-            q[i] = fast_silu(xq);
-            k[i] = fast_silu(xk);
+            q[i] = silu_fast(xq);
+            k[i] = silu_fast(xk);
             wq[i][0] = wq[i][1]; wq[i][1] = wq[i][2]; wq[i][2] = cur.q[i];
             wk[i][0] = wk[i][1]; wk[i][1] = wk[i][2]; wk[i][2] = cur.k[i];
             sq = fmaf(q[i], q[i], sq);
             sk = fmaf(k[i], k[i], sk);
             sqk = fmaf(q[i], k[i], sqk);
             al[i] = !a.kda ? alh
-                  : a.lb_gate ? __expf(lbv * fast_sigmoid(-A * cur.f[i]))
-                              : __expf(-A * fast_softplus(cur.f[i] + dtb[i]));
+                  : a.lb_gate ? __expf(lbv * sigmoid_fast(-A * cur.f[i]))
+                              : __expf(-A * softplus_fast(cur.f[i] + dtb[i]));
         }
         float vv = 0.f;
         if (vown) {
@@ -647,11 +629,11 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
             x = fmaf(cwv.y, wv[1], x);
             x = fmaf(cwv.z, wv[2], x);
             x = fmaf(cwv.w, cur.vz, x);
-            vv = fast_silu(x);
+            vv = silu_fast(x);
             wv[0] = wv[1]; wv[1] = wv[2]; wv[2] = cur.vz;
         }
         vv = __shfl_sync(FULL, vv, lane & ~1);
-        const float beta = fast_sigmoid(cur.beta);
+        const float beta = sigmoid_fast(cur.beta);
         const bool last = (t == Tb - 1);
         // the window after the last token (commit): every reader has passed the barrier above
         if (last && a.conv_out) {
@@ -756,7 +738,7 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
         for (int s = 0; s < NSLAB * NW; ++s) total += rms_slot[par][s];
         if (!klane && (lane & 1) == 0 && a.out) {
             const float rinv = rsqrtf(total * (1.0f / D) + a.eps_norm);
-            const float g = a.sig_gate ? fast_sigmoid(cur.vz) : fast_silu(cur.vz);
+            const float g = a.sig_gate ? sigmoid_fast(cur.vz) : silu_fast(cur.vz);
             const float y = o * rinv * nw * g;
             const size_t idx = bth * D + c0 + jc;
             if (a.out_bf16)

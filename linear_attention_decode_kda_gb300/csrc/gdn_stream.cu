@@ -228,7 +228,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
             const float4 *cwv = reinterpret_cast<const float4 *>(in + L.cw);
             // softplus gates: A = exp(A_log); lower-bound gate: A = the scale a
             const float A_raw = reinterpret_cast<const float *>(in + L.alog)[h & 3];
-            const float A = a.lb_gate ? A_raw : expf(A_raw);
+            const float A = a.lb_gate ? A_raw : __expf(A_raw);
             const int seg = qk_thr ? 0 : 2;  // q (and k) or v channels
             float w0[KM1], w1[KM1];
 #pragma unroll
@@ -249,8 +249,8 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
                 if (qk_thr) {
                     const float xq = smem_in(qkv, ch, a.in_bf16);
                     const float xk = smem_in(qkv, SD + ch, a.in_bf16);
-                    const float q = conv4_silu(cw0, w0, xq);
-                    const float kk = conv4_silu(cw1, w1, xk);
+                    const float q = conv4_silu_fast(cw0, w0, xq);
+                    const float kk = conv4_silu_fast(cw1, w1, xk);
                     w0[0] = w0[1]; w0[1] = w0[2]; w0[2] = xq;
                     w1[0] = w1[1]; w1[1] = w1[2]; w1[2] = xk;
                     sh.q[sl][ch] = q;
@@ -258,9 +258,9 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
                     float sq = q * q, sk = kk * kk, sqk = q * kk;
                     if (tid == 0) {
                         if (!a.kda)
-                            sh.a[sl][0] = expf(-A * softplus_f(smem_in(in + L.f + t * 16, h & (per16 - 1),
+                            sh.a[sl][0] = __expf(-A * softplus_fast(smem_in(in + L.f + t * 16, h & (per16 - 1),
                                                                        a.in_bf16) + dt));
-                        sh.beta[sl] = sigmoid_f(smem_in(in + L.beta + t * 16, h & (per16 - 1), a.in_bf16));
+                        sh.beta[sl] = sigmoid_fast(smem_in(in + L.beta + t * 16, h & (per16 - 1), a.in_bf16));
                     }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) {
@@ -276,13 +276,13 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
                 } else {
                     if (a.kda) {
                         const float fv = smem_in(in + L.f + t * SD * es, ch, a.in_bf16);
-                        sh.a[sl][ch] = a.lb_gate ? expf(dt * sigmoid_f(-A * fv)) : expf(-A * softplus_f(fv + dt));
+                        sh.a[sl][ch] = a.lb_gate ? __expf(dt * sigmoid_fast(-A * fv)) : __expf(-A * softplus_fast(fv + dt));
                     }
                     const float xv = smem_in(qkv, 2 * SD + ch, a.in_bf16);
-                    sh.v[sl][ch] = conv4_silu(cw0, w0, xv);
+                    sh.v[sl][ch] = conv4_silu_fast(cw0, w0, xv);
                     w0[0] = w0[1]; w0[1] = w0[2]; w0[2] = xv;
                     const float zv = smem_in(in + L.z + t * SD * es, ch, a.in_bf16);
-                    sh.gz[sl][ch] = nw * (a.sig_gate ? sigmoid_f(zv) : silu_f(zv));
+                    sh.gz[sl][ch] = nw * (a.sig_gate ? sigmoid_fast(zv) : silu_fast(zv));
                 }
                 if (a.conv_hist) {  // the window after token t
                     float *chh = a.conv_hist + (static_cast<size_t>(t) * a.B + b) * KM1 * C;
@@ -340,8 +340,8 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
                 Sk += sh.red3[sl][w][1];
                 Sqk += sh.red3[sl][w][2];
             }
-            const float rq = a.q_scale / sqrtf(Sq + a.eps_l2);
-            const float rk = 1.0f / sqrtf(Sk + a.eps_l2);
+            const float rq = a.q_scale * rsqrtf(Sq + a.eps_l2);
+            const float rk = rsqrtf(Sk + a.eps_l2);
             const float kq = Sqk * rq * rk;
 
             // B. decay and the two column reductions over this warp's 16 rows
@@ -393,7 +393,7 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
 
             // gated RMSNorm output, written by one warp per token
             if (a.out && warp == (t & (CW - 1))) {
-                const float rinv = 1.0f / sqrtf(p / static_cast<float>(SD) + a.eps_norm);
+                const float rinv = rsqrtf(p * (1.0f / SD) + a.eps_norm);
                 const float4 g4 = *reinterpret_cast<const float4 *>(&sh.gz[sl][col0]);
                 store_out4(a.out, e * SD + col0, a.out_bf16, o4.x * rinv * g4.x, o4.y * rinv * g4.y,
                            o4.z * rinv * g4.z, o4.w * rinv * g4.w);
