@@ -303,14 +303,18 @@ gdn_status_t gdn_layer_decode(const gdn_shape_t *s, const gdn_layer_weights_t *w
     for (const auto &d : gate)
         if (!gdn::proj_slot_ok(d)) return GDN_ERR_ALIGN;
     if (!gdn::proj_slot_ok(out[0])) return GDN_ERR_ALIGN;
-    if (gdn::launch_proj(in, 4, B, st) != cudaSuccess) return GDN_ERR_CUDA;
-    if (gdn::launch_proj(gate, 2, B, st) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_proj(in, 4, B, st, false) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_proj(gate, 2, B, st, true) != cudaSuccess) return GDN_ERR_CUDA;
     gdn::StepArgs a = step_args(s, t);
     a.state_out = t->state;
     a.conv_out = t->conv_state;
-    rc = run_step(s, a, st);
+    // The step overlaps its prologue with the projections before it, which write only
+    // the rows it reads after its dependency wait.
+    gdn_shape_t sp = *s;
+    sp.flags |= GDN_FLAG_PDL;
+    rc = run_step(&sp, a, st);
     if (rc != GDN_OK) return rc;
-    return gdn::launch_proj(out, 1, B, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return gdn::launch_proj(out, 1, B, st, true) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 const char *gdn_status_string(gdn_status_t status)

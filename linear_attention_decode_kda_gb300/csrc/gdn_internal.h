@@ -67,7 +67,11 @@ struct ProjSlotDesc {
     int N, K, ldx, ldy, x_bf16;
 };
 bool proj_slot_ok(const ProjSlotDesc &d);
-cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_t stream);
+// Launched with programmatic dependent launch (the kernels read activations and write
+// outputs after their dependency wait).  prefetch: below the tensor-core batch, ask L2
+// for the weights before that wait, for a launch that follows another kernel it can
+// overlap (the gate pair and the output projection of a layer).
+cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_t stream, bool prefetch);
 unsigned int take_proj_error();
 
 // Read and clear the step kernels' device error words (synchronous).
