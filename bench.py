@@ -258,16 +258,23 @@ class DecodeLayers(Workload):
         bf = s.bf16_in
         fw = s.f_width if s.kda else 1
 
-        def stack(field, width):
-            # [tokens, layers, B, width]
-            a = np.stack([getattr(x, field).reshape(s.B, self.tokens, width).swapaxes(0, 1)
-                          for x in ins], axis=1)
-            return np.ascontiguousarray(a)
-        host = {"qkv": stack("qkv", s.C), "f": stack("f", s.H_v * fw),
-                "beta": stack("beta", s.H_v), "z": stack("z", s.H_v * s.d_v)}
-        self.dev_in = {k: dev.to_torch(v, bf, device) for k, v in host.items()}
-        self.host_in = {k: dev.to_torch(v, bf, None).pin_memory() for k, v in host.items()}
-        del host
+        # One packed row per token: for each layer its qkv, f, beta and z rows, each
+        # segment padded to 16 bytes, so a token's inputs are one host-to-device copy.
+        widths = {"qkv": s.C, "f": s.H_v * fw, "beta": s.H_v, "z": s.H_v * s.d_v}
+        pad = 8 if bf else 4
+        self.seg = {}
+        off = 0
+        for k, w in widths.items():
+            self.seg[k] = (off, w)
+            off += -(-(s.B * w) // pad) * pad
+        packed = np.zeros((self.tokens, L, off), np.float32)
+        for k, (o, w) in self.seg.items():
+            for l, x in enumerate(ins):
+                a = getattr(x, k).reshape(s.B, self.tokens, w).swapaxes(0, 1)  # [tokens, B, w]
+                packed[:, l, o:o + s.B * w] = a.reshape(self.tokens, s.B * w)
+        self.dev_packed = dev.to_torch(packed, bf, device)
+        self.host_packed = dev.to_torch(packed, bf, None).pin_memory()
+        del packed
         self.cases = [dev.upload(s, params[l], synth.Inputs(ins[l].qkv[:, :1], ins[l].f[:, :1],
                                                               ins[l].beta[:, :1], ins[l].z[:, :1]),
                                  states[l], device=device) for l in range(L)]
@@ -275,18 +282,22 @@ class DecodeLayers(Workload):
         self.host_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         self.abi_shape = self.cases[0].abi_shape(pdl=pdl)
         self.kernel = gdn.gdn_kernel_variant(self.abi_shape, gdn.OP_DECODE)
-        self.h2d_bytes = sum(v[0].numel() * v.element_size() for v in self.dev_in.values())
+        self.h2d_bytes = self.dev_packed[0].numel() * self.dev_packed.element_size()
         self.d2h_bytes = self.out[0].numel() * 4
         self.graphs, self.e2e_graphs = {}, {}
         self.gdn = gdn
+
+    def _row(self, k, t, l):
+        o, w = self.seg[k]
+        return self.dev_packed[t, l, o:o + self.shape.B * w]
 
     def _launch_token(self, t):
         import torch
         st = torch.cuda.current_stream().cuda_stream
         for l, c in enumerate(self.cases):
             tens = self.gdn.tensors_from_torch(
-                qkv=self.dev_in["qkv"][t, l], f=self.dev_in["f"][t, l],
-                beta=self.dev_in["beta"][t, l], z=self.dev_in["z"][t, l], conv_w=c.conv_w,
+                qkv=self._row("qkv", t, l), f=self._row("f", t, l),
+                beta=self._row("beta", t, l), z=self._row("z", t, l), conv_w=c.conv_w,
                 A_log=c.A_log, dt_bias=c.dt_bias, norm_w=c.norm_w, conv_state=c.conv_state,
                 state=c.state, out=self.out[t, l])
             self.gdn.gdn_decode_step(self.abi_shape, tens, st)
@@ -302,8 +313,7 @@ class DecodeLayers(Workload):
             self.graphs[t] = g
             ge = torch.cuda.CUDAGraph()
             with torch.cuda.graph(ge):
-                for k in self.dev_in:
-                    self.dev_in[k][t].copy_(self.host_in[k][t], non_blocking=True)
+                self.dev_packed[t].copy_(self.host_packed[t], non_blocking=True)
                 self._launch_token(t)
                 self.host_out[t].copy_(self.out[t], non_blocking=True)
             self.e2e_graphs[t] = ge
