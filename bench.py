@@ -238,6 +238,26 @@ def _dev_inputs(shape, layers, tokens, seed=0, slow=False):
     return params, states, ins
 
 
+def pack_token_inputs(shape, ins, tokens):
+    """Per-layer input arrays -> one packed row per token: [tokens, layers, row] fp32, the
+    row holding qkv, f, beta and z of one layer ([B, width] each, token t), every segment
+    padded to 16 bytes of the input dtype.  Returns (packed, {name: (offset, width)})."""
+    s = shape
+    fw = s.f_width if s.kda else 1
+    widths = {"qkv": s.C, "f": s.H_v * fw, "beta": s.H_v, "z": s.H_v * s.d_v}
+    pad = 8 if s.bf16_in else 4
+    seg, off = {}, 0
+    for k, w in widths.items():
+        seg[k] = (off, w)
+        off += -(-(s.B * w) // pad) * pad
+    packed = np.zeros((tokens, len(ins), off), np.float32)
+    for k, (o, w) in seg.items():
+        for l, x in enumerate(ins):
+            a = getattr(x, k).reshape(s.B, tokens, w).swapaxes(0, 1)  # [tokens, B, w]
+            packed[:, l, o:o + s.B * w] = a.reshape(tokens, s.B * w)
+    return packed, seg
+
+
 class DecodeLayers(Workload):
     """B sequences x `layers` independent layers, one token per step (graphs per token)."""
 
@@ -256,22 +276,9 @@ class DecodeLayers(Workload):
         self.bytes_per_launch = algorithmic_bytes(s)
         params, states, ins = _dev_inputs(s, L, self.tokens)
         bf = s.bf16_in
-        fw = s.f_width if s.kda else 1
-
-        # One packed row per token: for each layer its qkv, f, beta and z rows, each
-        # segment padded to 16 bytes, so a token's inputs are one host-to-device copy.
-        widths = {"qkv": s.C, "f": s.H_v * fw, "beta": s.H_v, "z": s.H_v * s.d_v}
-        pad = 8 if bf else 4
-        self.seg = {}
-        off = 0
-        for k, w in widths.items():
-            self.seg[k] = (off, w)
-            off += -(-(s.B * w) // pad) * pad
-        packed = np.zeros((self.tokens, L, off), np.float32)
-        for k, (o, w) in self.seg.items():
-            for l, x in enumerate(ins):
-                a = getattr(x, k).reshape(s.B, self.tokens, w).swapaxes(0, 1)  # [tokens, B, w]
-                packed[:, l, o:o + s.B * w] = a.reshape(self.tokens, s.B * w)
+        # One packed row per token (all layers' qkv, f, beta and z), so a token's inputs
+        # are one host-to-device copy.
+        packed, self.seg = pack_token_inputs(s, ins, self.tokens)
         self.dev_packed = dev.to_torch(packed, bf, device)
         self.host_packed = dev.to_torch(packed, bf, None).pin_memory()
         del packed
