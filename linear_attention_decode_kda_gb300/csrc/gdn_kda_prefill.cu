@@ -61,6 +61,12 @@ __device__ unsigned int g_kda_error;
 // Intra kernel staging rows: 136 floats, 4 spare after channel 63, so the two
 // channel halves of a row sit in different banks.
 constexpr int SP = 136;
+// fp32 rows of [W; e^G Q] before their split into the canonical layout: a stride of
+// 132 floats (4 banks on a row) lets 8 rows' 16-byte pieces be read without conflict.
+constexpr int FS = 132;
+// dynamic shared memory of the intra kernel: the staging rows, then the W/Q rows
+constexpr int INTRA_STG = 4 * KC * SP * 4;
+constexpr int INTRA_SMEM = INTRA_STG + 2 * KC * FS * 4;
 __device__ __forceinline__ int hp(int i) { return i + ((i >> 6) << 2); }
 
 // SiLU and sigmoid on the fast exponential and division: within a few units in
@@ -117,7 +123,9 @@ kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensor
                  const __grid_constant__ CUtensorMap tf)
 {
     // staging rows of q, k, v and G; they take the block image at the end
-    __shared__ __align__(128) float stg[4][KC][SP];
+    extern __shared__ __align__(1024) unsigned char ism[];
+    float(*stg)[KC][SP] = reinterpret_cast<float(*)[KC][SP]>(ism);
+    float(*fwq)[FS] = reinterpret_cast<float(*)[FS]>(ism + INTRA_STG);
     __shared__ uint64_t raw_bar;
     float(*qs)[SP] = stg[0];
     float(*ks)[SP] = stg[1];
@@ -382,13 +390,26 @@ kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensor
         }
     }
     const float m = As[tid >> 4][tid & 15];
+    if (tid < KD)
+#pragma unroll
+        for (int t = 0; t < KC; ++t) {
+            fwq[t][i] = x[t];
+            fwq[KC + t][i] = y[t];
+        }
     __syncthreads();  // the staging rows are read: they take the block image
     unsigned char *img = reinterpret_cast<unsigned char *>(&stg[0][0][0]);
     if (tid < KD) {
+        // [W; e^G Q] split into fp16 hi/lo: one 8-row x 8-channel core matrix per 8
+        // threads (8 rows of one channel group), 16-byte reads and writes
 #pragma unroll
-        for (int t = 0; t < KC; ++t) {
-            tc::put_split(img + BW_WQ, img + BW_WQ + 8192, tc::op_offset(t, i, KD), x[t]);
-            tc::put_split(img + BW_WQ, img + BW_WQ + 8192, tc::op_offset(KC + t, i, KD), y[t]);
+        for (int e = 0; e < 4; ++e) {
+            const int r = 8 * e + (tid & 7), c8 = 8 * (tid >> 3);
+            float v8[8];
+            const float4 u0 = *reinterpret_cast<const float4 *>(&fwq[r][c8]);
+            const float4 u1 = *reinterpret_cast<const float4 *>(&fwq[r][c8 + 4]);
+            v8[0] = u0.x; v8[1] = u0.y; v8[2] = u0.z; v8[3] = u0.w;
+            v8[4] = u1.x; v8[5] = u1.y; v8[6] = u1.z; v8[7] = u1.w;
+            tc::put_row8(img + BW_WQ, img + BW_WQ + 8192, tc::op_offset(r, c8, KD), v8);
         }
     } else {
         float *U = reinterpret_cast<float *>(img + BW_U);
@@ -740,6 +761,17 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(kda_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
+        // the intra kernel's rows exceed the 48 KB default; four CTAs an SM keep their share
+        void (*intra[4])(StepArgs, unsigned char *, CUtensorMap, CUtensorMap) = {
+            kda_intra_kernel<true, true>, kda_intra_kernel<true, false>,
+            kda_intra_kernel<false, true>, kda_intra_kernel<false, false>};
+        for (auto fn : intra) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, INTRA_SMEM);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+        }
         attr_set[dev] = true;
     }
     const int nchunk = (a.T + KC - 1) / KC;
@@ -773,13 +805,13 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
     }
     const dim3 grid(nchunk, a.H_v, a.B);
     if (a.in_bf16 && a.kda)
-        kda_intra_kernel<true, true><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
+        kda_intra_kernel<true, true><<<grid, 256, INTRA_SMEM, stream>>>(a, ws, tq, tf);
     else if (a.in_bf16)
-        kda_intra_kernel<true, false><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
+        kda_intra_kernel<true, false><<<grid, 256, INTRA_SMEM, stream>>>(a, ws, tq, tf);
     else if (a.kda)
-        kda_intra_kernel<false, true><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
+        kda_intra_kernel<false, true><<<grid, 256, INTRA_SMEM, stream>>>(a, ws, tq, tf);
     else
-        kda_intra_kernel<false, false><<<grid, 256, 0, stream>>>(a, ws, tq, tf);
+        kda_intra_kernel<false, false><<<grid, 256, INTRA_SMEM, stream>>>(a, ws, tq, tf);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kda_state_kernel<<<dim3(a.H_v, a.B), ST_THREADS, SMEM, stream>>>(a, ws, nchunk, tmz);
