@@ -804,6 +804,9 @@ bool plan_slab(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
         best = nslab;
         if (units * nslab >= 2L * num_sms) break;
     }
+    // d = 128 from 64 units: two slabs a head measured fastest (B2 H32: 5.2 us a launch,
+    // against 5.5 with four and 5.6 with eight; B1 is within 1% for 2, 4 or 8 slabs).
+    if (D == 128 && units >= 64 && 2 * group <= 8) best = 2;
     if (best == 0) return false;
     const Variant *v = find_variant(D, D / best);
     plan->kind = StepPlan::kSlab;
@@ -897,10 +900,10 @@ bool plan_wstep(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
     (void)num_sms;
     if (D != WD || group < 1 || group > 8) return false;
     const long units = static_cast<long>(B) * H_v;
-    // Below 128 units the column-slab kernel, whose 8-way slabs spread a head's state
-    // over more SMs, keeps the shorter chain (B1 H32: 5.2 against 5.3 us a launch; B2:
-    // 6.0 against 6.7).  From 128 units two 64-column slabs a head measured fastest
-    // (B4 H32: 8.4 us, against 11.1 on the slab kernel and 9.0 with whole heads).
+    // Below 128 units the column-slab kernel keeps the shorter chain (B1 H32: 4.4
+    // against 5.8 us a launch; B2: 5.2 against 6.8).  From 128 units two 64-column
+    // slabs a head measured fastest (B4 H32: 8.8 us, against 10.1 on the slab kernel
+    // and 9.1 with whole heads; B8: 17.3 against 20.1).
     if (units < 128) return false;
     const int best = 2 * group <= 8 ? 2 : 1;
     const WVariant *v = find_wvariant(D / best);
