@@ -17,8 +17,9 @@ time is the sum of the K step times.  `e2e` repeats the steps through the same
 C ABI with the step's inputs copied from pinned host memory and its outputs
 copied back inside the timed region.
 
-`--impl reference` times the fp64 CPU oracle (the reference of this build) on
-the host cores for the same workload and metric.
+`--impl reference` times the fp64 CPU oracle (the slow reference arm: there is no
+installable implementation of the method to compare against) on the host cores
+for the same workload and metric.
 """
 
 from __future__ import annotations
