@@ -185,6 +185,24 @@ def test_variant_choice(lib):
     assert gdn.gdn_kernel_variant(_shape(d_k=48, d_v=48), gdn.OP_DECODE) is None
 
 
+@pytest.mark.parametrize("B,H_qk,H_v,want", [
+    (1, 32, 32, "step<128,16>"),     # below 64 units: the 8-slab plan
+    (2, 32, 32, "step<128,64>"),     # 64 to 127 units: two slabs a head
+    (3, 32, 32, "step<128,64>"),
+    (3, 8, 16, "step<128,32>"),      # 48 grouped units: slabs x group within a cluster of 8
+    (4, 32, 32, "wstep<128,64>"),    # from 128 units: the warp-column kernel, two slabs
+    (9, 32, 32, "wstep<128,64>"),
+    (10, 32, 32, "stream<128>"),     # two units an SM: the streaming kernel
+    (4, 8, 32, "wstep<128,64>"),     # grouped heads never stream
+    (2, 8, 64, "wstep<128,128>"),    # a group of 8 value heads: whole heads a CTA
+])
+def test_decode_routing_by_unit_count(lib, B, H_qk, H_v, want):
+    """The d = 128 decode plan by (sequence, head) units (148 SMs when no GPU is present,
+    152 on a GB300: the thresholds below sit away from both)."""
+    for op in (gdn.OP_DECODE, gdn.OP_VERIFY):
+        assert gdn.gdn_kernel_variant(_shape(B=B, H_qk=H_qk, H_v=H_v), op) == want
+
+
 def test_product_path_never_touches_the_oracle():
     """The package and its CUDA sources import / include nothing from oracle/."""
     pkg = os.path.join(ROOT, "linear_attention_decode_kda_gb300")
