@@ -382,16 +382,17 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         //    token ahead of the slowest (it needs every partial to finish a token).
         float p = 0.f;
         if (warp == 0) {
+            // the slab's columns sit on lanes 0..TPR-1 of warp 0
             if (rg == 0) p = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            for (int off = TPR >> 1; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            p = __shfl_sync(0xffffffffu, p, 0);
         }
         float total = p;
         if (clustered) {
-            if (tid == 0) {
-                mbar_expect_tx(&rms_bar[t & 1], NSLAB * 4);
-#pragma unroll
-                for (int s = 0; s < NSLAB; ++s) st_async_remote(&rms_slot[t & 1][slab], rank0 + s, p, &rms_bar[t & 1]);
+            if (warp == 0) {  // lane s pushes to slab s
+                if (lane == 0) mbar_expect_tx(&rms_bar[t & 1], NSLAB * 4);
+                if (lane < NSLAB) st_async_remote(&rms_slot[t & 1][slab], rank0 + lane, p, &rms_bar[t & 1]);
             }
             if (rg == 0) {
                 ok &= mbar_wait_cluster_bounded(&rms_bar[t & 1], static_cast<uint32_t>(t >> 1) & 1u);
