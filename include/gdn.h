@@ -245,6 +245,13 @@ typedef struct {
  * conv_state and state are the step's.  gate_mode must be a per-channel gate.
  * workspace holds gdn_layer_workspace_bytes bytes (the low-rank rows),
  * 16-byte aligned.  x_out is [B][d_model] fp32.
+ *
+ * The four launches use programmatic dependent launch whatever shape->flags
+ * holds: each kernel reads activations and writes its outputs only after the
+ * previous kernel on the stream has completed, and before that touches nothing
+ * but read-only weights (asked into L2) and, for the step, its own state,
+ * window and parameters.  The first projection therefore needs no promise from
+ * the caller about the kernel before it.
  */
 GDN_API gdn_status_t gdn_layer_decode(const gdn_shape_t *shape, const gdn_layer_weights_t *w,
                               const void *x, float *x_out, const gdn_tensors_t *t,
