@@ -150,8 +150,10 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = ps.tmem;
-    pdl_launch_dependents();
     pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    pdl_launch_dependents();
 
     // parameters and conv windows: half 0 convolves q and k of channel ch, half 1 v
     const float A_h = expf(a.A_log[h]);

@@ -91,7 +91,6 @@ __device__ __forceinline__ void load_x8(const void *x, size_t idx, int bf16, flo
 template <int NB>
 __global__ void __launch_bounds__(PT) proj_kernel(const __grid_constant__ Args p)
 {
-    dev::pdl_launch_dependents();
     // Before the dependency wait: the first pf_ctas CTAs (those that start early, beside
     // the previous kernel) ask L2 for the rows of CTAs c, c + pf_ctas, ...
     if (threadIdx.x < 32 && static_cast<int>(blockIdx.x) < p.pf_ctas) {
@@ -117,6 +116,9 @@ __global__ void __launch_bounds__(PT) proj_kernel(const __grid_constant__ Args p
     const int nk = s.K / 8;
     const uint4 *wr = reinterpret_cast<const uint4 *>(s.w + static_cast<size_t>(valid ? n : 0) * s.K);
     dev::pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    dev::pdl_launch_dependents();
 
     for (int b0 = 0; b0 < p.B; b0 += NB) {
         float acc[NB];
@@ -256,7 +258,6 @@ proj_tc_kernel(const __grid_constant__ Args p, const __grid_constant__ TcMaps ma
     const int nk = s.K / TC_K / p.ksplit;                           // K tiles of this CTA
     const int kt0 = blockIdx.z * nk;                                 // its first K tile
 
-    dev::pdl_launch_dependents();
     if (warp == 0) tc::tmem_alloc(&ts.tmem, TC_N);
     if (tid == 0) {
         for (int i = 0; i < NS; ++i) {
@@ -283,6 +284,9 @@ proj_tc_kernel(const __grid_constant__ Args p, const __grid_constant__ TcMaps ma
     // Asking L2 for the weights before the wait measured slower here (B64 layer: 150.8
     // against 146.7 us): the TMA ring already keeps the weight stream busy.
     dev::pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    dev::pdl_launch_dependents();
     if (tid == 0) {
         dev::prefetch_tensormap(mw);
         dev::prefetch_tensormap(mx);

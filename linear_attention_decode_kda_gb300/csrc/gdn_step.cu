@@ -91,7 +91,6 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     __shared__ __align__(8) uint64_t rms_bar[2];  // completed by the slabs' pushes of token parity
     __shared__ float beta_s;
 
-    pdl_launch_dependents();
     uint32_t rank0 = 0;  // cluster rank of slab 0 of this head
     if (clustered) {
         rank0 = cluster_rank() - slab;
@@ -186,6 +185,9 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
 
     // ---- inputs may be written by the previous kernel on the stream
     pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    pdl_launch_dependents();
 
     // All inputs of token t in one round of independent loads.
     auto load_token = [&](int t, TokenIn<CQ, CV> &in) {
@@ -488,7 +490,6 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
     __shared__ float rms_slot[2][NSLAB * NW];  // the warps' sums of o^2, by token parity
     __shared__ __align__(8) uint64_t rms_bar[2];
 
-    pdl_launch_dependents();
     uint32_t rank0 = 0;  // cluster rank of slab 0 of this head
     if (NSLAB > 1 || clustered) {
         rank0 = cluster_rank() - slab;
@@ -572,6 +573,9 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
 
     // ---- inputs may be written by the previous kernel on the stream
     pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    pdl_launch_dependents();
 
     auto load_token = [&](int t, WIn &in) {
         const size_t bt = static_cast<size_t>(b) * a.T + t;

@@ -177,7 +177,6 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_launch_dependents();
     // The state is not written by the previous kernel on the stream (launch
     // contract): the first tile is requested before the dependency wait.
     if (tid == 0) {
@@ -193,6 +192,9 @@ stream_kernel(const StepArgs a, const __grid_constant__ InMaps maps, int n_heads
         prefetch_tensormap(&maps.beta);
     }
     pdl_wait();  // inputs may be written by the previous kernel on the stream
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    pdl_launch_dependents();
     if (warp == 0) {
         for (int s = 0; s < nst; ++s) {
             const int j = c0 + s * G;
