@@ -135,9 +135,9 @@ def kernel_source_hash(files=None) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, path: str = None):
     """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    p = path or os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(workload)

@@ -43,3 +43,24 @@ def test_packed_rows_round_trip(B, kda, bf16):
     ends.sort()
     for (a0, a1), (b0, _) in zip(ends, ends[1:]):
         assert a1 <= b0, "segments overlap"
+
+
+def test_traffic_figures_only_for_unchanged_sources(tmp_path):
+    """A DRAM-traffic figure is reported only while the sources of the workload's kernels
+    hash to the value recorded with it; any other hash, or a missing entry, gives None."""
+    import json
+    w = "kda_decode_b64"
+    good = bench.kernel_source_hash(bench.workload_sources(w))
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps({w: {"dram_bytes_per_launch": 123, "source_sha256_16": good},
+                             "kda_verify_b32_t4": {"dram_bytes_per_launch": 7,
+                                                   "source_sha256_16": "0" * 16}}))
+    assert bench.ncu_traffic(w, str(f)) == 123
+    assert bench.ncu_traffic("kda_verify_b32_t4", str(f)) is None
+    assert bench.ncu_traffic("kda_commit_b32_t4", str(f)) is None
+    assert bench.ncu_traffic(w, str(tmp_path / "missing.json")) is None
+    # each workload hashes the sources its kernels are built from
+    assert "gdn_step.cu" in bench.workload_sources("kda_decode_b1_34layers")
+    assert "gdn_stream.cu" in bench.workload_sources(w)
+    assert "gdn_kda_prefill.cu" in bench.workload_sources("kda_prefill_b4_t4096")
+    assert "gdn_proj.cu" in bench.workload_sources("kda_layer_decode_b1")
