@@ -1,6 +1,10 @@
-"""The bench's end-to-end input layout on CPU: one packed row per token holds every
-layer's qkv, f, beta and z rows, each segment on a 16-byte boundary, and slicing the
-row gives back exactly the arrays the layers were generated with."""
+"""The bench's host logic on CPU.
+
+- The end-to-end input layout: one packed row per token holds every layer's qkv, f, beta
+  and z rows, each segment on a 16-byte boundary. Slicing the row gives back exactly the
+  arrays the layers were generated with.
+- The DRAM-traffic figures: reported only for the kernel sources they were taken on.
+"""
 
 import dataclasses
 import os
