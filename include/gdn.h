@@ -80,11 +80,16 @@ enum {
     /*
      * Launch with programmatic dependent launch: the kernel reads `state`,
      * `conv_state` and the parameters before it waits for the previous kernel
-     * on the stream, and lets the next kernel start early.  The caller
-     * asserts that the kernel queued just before this call on the stream does
-     * not write `state`, `conv_state` or the parameters (for example, the
-     * previous layer of a model).  Inputs q/k/v/f/beta/z are read after the
-     * wait.  Without this flag launches are plain stream-ordered.
+     * on the stream, and lets the next kernel start once its own wait has
+     * returned.  The caller asserts that the kernel queued just before this
+     * call on the stream does not write `state`, `conv_state` or the
+     * parameters (for example, the previous layer of a model).  If that kernel
+     * lets its dependents start before its own dependency wait, the same must
+     * hold for the kernels before it that may still be running.  This
+     * library's kernels let their dependents start only after their own wait,
+     * so a chain of its calls needs the promise for the immediately preceding
+     * call alone.  Inputs q/k/v/f/beta/z are read after the wait.  Without
+     * this flag launches are plain stream-ordered.
      */
     GDN_FLAG_PDL = 1,
     /* Output gate sigmoid(z) in place of silu(z). */
