@@ -203,6 +203,29 @@ def test_decode_routing_by_unit_count(lib, B, H_qk, H_v, want):
         assert gdn.gdn_kernel_variant(_shape(B=B, H_qk=H_qk, H_v=H_v), op) == want
 
 
+def test_dependents_start_only_after_the_dependency_wait():
+    """Every kernel that takes part in programmatic dependent launch lets its dependents
+    start only after its own dependency wait: in each kernel body the trigger follows the
+    wait.  A trigger before the wait would let a dependent's pre-wait reads run beside a
+    kernel earlier than its immediate predecessor."""
+    csrc = os.path.join(ROOT, "linear_attention_decode_kda_gb300", "csrc")
+    seen = 0
+    for fn in sorted(os.listdir(csrc)):
+        if not fn.endswith(".cu"):
+            continue
+        text = open(os.path.join(csrc, fn)).read()
+        for body in re.split(r"__global__", text)[1:]:
+            trig = [m.start() for m in re.finditer(r"pdl_launch_dependents\(\)", body)]
+            wait = [m.start() for m in re.finditer(r"pdl_wait\(\)", body)]
+            if not trig:
+                continue
+            seen += 1
+            assert wait, f"{fn}: a kernel triggers dependents without a dependency wait"
+            # only the first kernel body after each __global__ up to the next one is scanned
+            assert min(trig) > min(wait), f"{fn}: dependents triggered before the wait"
+    assert seen >= 6, seen
+
+
 def test_product_path_never_touches_the_oracle():
     """The package and its CUDA sources import / include nothing from oracle/."""
     pkg = os.path.join(ROOT, "linear_attention_decode_kda_gb300")
