@@ -80,21 +80,13 @@ def prefill_flops(s: synth.Shape) -> float:
     return float(s.B * nch * (s.H_v * per_v + s.H_qk * per_qk))
 
 
-# fp32 FMA peak of the part: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (maximum SM
-# clock).  The two-kernel chunked prefill runs its products on these lanes.
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-
-
-def two_kernel_flops(s: synth.Shape, C: int = 16):
-    """(tensor, fp32) FLOPs of the two-kernel chunked form at chunk C, per
-    (sequence, value head, chunk): the state kernel's tcgen05 products W S, e^G Q S
-    and the state update (2 C d^2 each) and A V_new (2 C^2 d); the intra kernel's
-    fp32 pair sums K K^T and Q K^T over the lower triangle (C^2 d each) and the
-    forward substitution on 2d columns (C^2 d each side)."""
+def two_kernel_flops(s: synth.Shape, C: int = 16) -> float:
+    """Tensor-core FLOPs of the two-kernel chunked form at chunk C, per (sequence,
+    value head, chunk): the state kernel's tcgen05 products W S, e^G Q S and the state
+    update (2 C d^2 each) and A V_new (2 C^2 d)."""
     d = s.d_k
     units = s.B * s.H_v * -(-s.T // C)
-    return (float(units * (3 * 2 * C * d * d + 2 * C * C * d)),
-            float(units * (2 * C * C * d + 2 * C * C * d)))
+    return float(units * (3 * 2 * C * d * d + 2 * C * C * d))
 
 
 def measured_peaks() -> dict:
@@ -107,7 +99,7 @@ def measured_peaks() -> dict:
 
 # The sources each workload's kernels are built from: a traffic figure stays valid
 # while these files are unchanged.
-_COMMON_SOURCES = ("gdn_api.cu", "gdn_internal.h", "gdn_device.cuh")
+_COMMON_SOURCES = ("gdn_internal.h", "gdn_device.cuh")
 _STREAM_SOURCES = _COMMON_SOURCES + ("gdn_stream.cu", "gdn_tmap.cu", "gdn_tmap.h")
 _STEP_SOURCES = _COMMON_SOURCES + ("gdn_step.cu",)
 _PREFILL_SOURCES = _COMMON_SOURCES + ("gdn_kda_prefill.cu", "gdn_prefill.cu", "gdn_prefill.h",
@@ -292,7 +284,7 @@ class DecodeLayers(Workload):
         self.kernel = gdn.gdn_kernel_variant(self.abi_shape, gdn.OP_DECODE)
         self.h2d_bytes = self.dev_packed[0].numel() * self.dev_packed.element_size()
         self.d2h_bytes = self.out[0].numel() * 4
-        self.graphs, self.e2e_graphs = {}, {}
+        self.graphs, self.e2e_graphs, self.eager_tensors = {}, {}, {}
         self.gdn = gdn
 
     def _row(self, k, t, l):
@@ -302,19 +294,22 @@ class DecodeLayers(Workload):
     def _launch_token(self, t):
         import torch
         st = torch.cuda.current_stream().cuda_stream
-        for l, c in enumerate(self.cases):
-            tens = self.gdn.tensors_from_torch(
-                qkv=self._row("qkv", t, l), f=self._row("f", t, l),
-                beta=self._row("beta", t, l), z=self._row("z", t, l), conv_w=c.conv_w,
-                A_log=c.A_log, dt_bias=c.dt_bias, norm_w=c.norm_w, conv_state=c.conv_state,
-                state=c.state, out=self.out[t, l])
-            self.gdn.gdn_decode_step(self.abi_shape, tens, st)
+        for l in range(len(self.cases)):
+            self.gdn.gdn_decode_step(self.abi_shape, self._tensors(t, l), st)
+
+    def _tensors(self, t, l):
+        c = self.cases[l]
+        return self.gdn.tensors_from_torch(
+            qkv=self._row("qkv", t, l), f=self._row("f", t, l), beta=self._row("beta", t, l),
+            z=self._row("z", t, l), conv_w=c.conv_w, A_log=c.A_log, dt_bias=c.dt_bias,
+            norm_w=c.norm_w, conv_state=c.conv_state, state=c.state, out=self.out[t, l])
 
     def capture(self, tokens):
         import torch
         for t in tokens:
             if t in self.graphs:
                 continue
+            self.eager_tensors[t] = [self._tensors(t, l) for l in range(len(self.cases))]
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 self._launch_token(t)
@@ -329,8 +324,19 @@ class DecodeLayers(Workload):
     def step(self, i):
         self.graphs[i % self.tokens].replay()
 
-    def e2e_step(self, i):
+    def e2e_graph_step(self, i):
         self.e2e_graphs[i % self.tokens].replay()
+
+    def e2e_step(self, i):
+        """The token's inputs copied in, one gdn_decode_step call per layer through the
+        C ABI (host checks and launch included), the outputs copied back."""
+        import torch
+        t = i % self.tokens
+        st = torch.cuda.current_stream().cuda_stream
+        self.dev_packed[t].copy_(self.host_packed[t], non_blocking=True)
+        for tens in self.eager_tensors[t]:
+            self.gdn.gdn_decode_step(self.abi_shape, tens, st)
+        self.host_out[t].copy_(self.out[t], non_blocking=True)
 
 
 class SingleLaunch(Workload):
@@ -376,9 +382,8 @@ class SingleLaunch(Workload):
         self.flops_per_launch = (prefill_flops(dataclasses.replace(s, chunk=int(m.group(1))))
                                  if m else 0.0)
         m = re.match(r"kda_chunked<(\d+)>", self.kernel or "") if op == gdn.OP_PREFILL else None
-        self.alu_flops_per_launch = 0.0
         if m:
-            self.flops_per_launch, self.alu_flops_per_launch = two_kernel_flops(s, int(m.group(1)))
+            self.flops_per_launch = two_kernel_flops(s, int(m.group(1)))
         self.ws_bytes = gdn.gdn_prefill_workspace_bytes(self.abi_shape) if op == 2 else 0
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
         self.h2d_bytes = sum(v[0].numel() * v.element_size() for v in self.dev_in.values())
@@ -553,6 +558,11 @@ def time_steps(fn, warmup, steps, flush):
     return float(sum(a.elapsed_time(b) for a, b in ev))
 
 
+# Nominal HBM3e bandwidth of the part (about 8 TB/s).  The roofline fraction divides by
+# the measured copy bandwidth; frac_nominal divides by this figure, the harder bar.
+NOMINAL_HBM_GBS = 8000.0
+
+
 def roofline(w: Workload, ms_per_step: float, peaks: dict) -> dict:
     per_launch_s = ms_per_step * 1e-3 / w.launches_per_step
     achieved = w.bytes_per_launch / per_launch_s / 1e9
@@ -560,7 +570,24 @@ def roofline(w: Workload, ms_per_step: float, peaks: dict) -> dict:
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": ncu_traffic(w.name), "kernel": w.kernel,
             "algorithmic_bytes_per_launch": w.bytes_per_launch,
-            "peak_source": peaks["src"] + " copy bandwidth"}
+            "peak_source": peaks["src"] + " copy bandwidth",
+            "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "peak_nominal": NOMINAL_HBM_GBS}
+
+
+def workload_entry(w: Workload, wms: float, peaks: dict) -> dict:
+    """One workload's figures, short keys so the whole line stays a few KB:
+    v layer-steps/s, us per call, frac of the measured copy peak achieved over the
+    algorithmic bytes, fnom the same of the nominal 8 TB/s, tr ncu DRAM bytes per call
+    (null when not taken on the current sources), k the kernel; prefill adds tc, the
+    fraction of the bf16 tensor peak of the chunked form's dense products."""
+    r = roofline(w, wms, peaks)
+    e = {"v": round(w.units_per_step / (wms * 1e-3), 1), "us": round(wms * 1e3, 2),
+         "frac": r["frac"], "fnom": r["frac_nominal"], "tr": r["traffic"], "k": w.kernel}
+    if getattr(w, "flops_per_launch", 0):
+        tf = w.flops_per_launch / (wms * 1e-3) / 1e12
+        e["tc"] = round(tf / peaks["bf16_tflops"], 4)
+    return e
 
 
 # ---------------------------------------------------------------- CPU oracle legs
@@ -596,9 +623,22 @@ def oracle_decode_rate(name: str, tokens: int, nthreads: int, target_s: float = 
     steps = passes * layers * s.B * tokens
     return {"value": round(steps / dt, 2), "unit": UNIT,
             "cores": min(nthreads, s.B * s.H_v), "kind": "oracle",
-            "sample": f"{passes} passes x {layers} layers x {tokens} tokens of {name} "
-                      f"(fp64 C, threads over (sequence, head) units; state carried)",
+            "sample": f"{passes} passes x {layers} layers x {tokens} tokens, fp64 C, "
+                      f"threads over units",
             "seconds": round(dt, 2)}
+
+
+def cpu_baseline(name: str, tokens: int, nthreads: int) -> dict:
+    """The oracle on every host core (about 12 s) and on one thread (about 6 s), with
+    the effective GB/s over the same algorithmic bytes per layer-step as the GPU line."""
+    multi = oracle_decode_rate(name, tokens, nthreads)
+    single = oracle_decode_rate(name, tokens, 1, target_s=6.0)
+    per_step = algorithmic_bytes(synth.WORKLOADS[name]["shape"]) / synth.WORKLOADS[name]["shape"].B
+    multi["gbs"] = round(multi["value"] * per_step / 1e9, 2)
+    multi["single_thread"] = {"value": single["value"], "unit": UNIT, "cores": 1,
+                              "gbs": round(single["value"] * per_step / 1e9, 3),
+                              "seconds": single["seconds"]}
+    return multi
 
 
 def run_reference(args):
@@ -695,7 +735,9 @@ def run_ours(args):
     with ClockSampler(str(uuid) if uuid else None) as clk:
         ms = time_steps(main.step, args.warmup, args.steps, flush)
     ms_e2e = time_steps(main.e2e_step, args.warmup, args.steps, flush)
-    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, device)
+    graph_leg = getattr(main, "e2e_graph_step", None)
+    ms_e2e_graph = time_steps(graph_leg, args.warmup, args.steps, flush) if graph_leg else 0.0
+    ms, ms_e2e, ms_e2e_graph = max_over_ranks([ms, ms_e2e, ms_e2e_graph], world, device)
     if world > 1:
         dist.barrier()
 
@@ -711,8 +753,8 @@ def run_ours(args):
                        "gate": "per-channel (KDA)" if main.shape.kda else "per-head (GDN)",
                        "inputs": "bf16" if main.shape.bf16_in else "f32",
                        "state": "f32", "out": "f32",
-                       "l2": f"flushed ({FLUSH_BYTES >> 20} MiB memset) before every step",
-                       "launch": "CUDA graph per token, programmatic dependent launch"
+                       "l2": f"{FLUSH_BYTES >> 20} MiB memset before each step",
+                       "launch": "graph per token, PDL"
                        if isinstance(main, DecodeLayers) else "one ABI call per step",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline(main, ms_step, peaks),
@@ -721,6 +763,10 @@ def run_ours(args):
                     "h2d_bytes_per_step": main.h2d_bytes, "d2h_bytes_per_step": main.d2h_bytes},
             "gpu_launches": main.launches_per_step * getattr(main, "kernels_per_launch", 1) * args.steps,
             "clocks": clk.summary()}
+    if graph_leg:
+        # the same copies and launches replayed from a CUDA graph captured per token
+        line["e2e_graph"] = {"value": round(whole_job_rate(main.units_per_step, args.steps, world,
+                                                           ms_e2e_graph), 2), "unit": UNIT}
 
     if rank == 0 and not args.no_workloads:
         extra = {}
@@ -732,27 +778,14 @@ def run_ours(args):
             w = make_workload(name, device)
             k = args.aux_steps if name not in PREFILL_WORKLOADS else max(3, args.aux_steps // 10)
             wms = time_steps(w.step, 3, k, flush) / k
-            r = roofline(w, wms, peaks)
-            entry = {"value": round(w.units_per_step / (wms * 1e-3), 1), "unit": UNIT,
-                     "ms_per_step": round(wms, 5), "kernel": w.kernel, "roofline": r}
-            if getattr(w, "alu_flops_per_launch", 0):
-                tf = w.alu_flops_per_launch / (wms * 1e-3) / 1e12
-                entry["alu"] = {"achieved": round(tf, 2), "peak": round(FP32_PEAK_TFLOPS, 1),
-                                "unit": "TFLOP/s", "frac": round(tf / FP32_PEAK_TFLOPS, 4),
-                                "peak_from": "152 SMs x 128 fp32 lanes x 2 x 2.07 GHz"}
-            if getattr(w, "flops_per_launch", 0):
-                tf = w.flops_per_launch / (wms * 1e-3) / 1e12
-                entry["tensor"] = {"achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
-                                   "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4)}
-            extra[name] = entry
+            extra[name] = workload_entry(w, wms, peaks)
             del w
             torch.cuda.empty_cache()
         line["workloads"] = extra
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_decode_rate(main.name if isinstance(main, DecodeLayers)
-                                                  else DEFAULT_WORKLOAD, args.cpu_tokens,
-                                                  os.cpu_count() or 1)
+        name = main.name if isinstance(main, DecodeLayers) else DEFAULT_WORKLOAD
+        line["cpu_baseline"] = cpu_baseline(name, args.cpu_tokens, os.cpu_count() or 1)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

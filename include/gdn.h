@@ -200,8 +200,12 @@ GDN_API size_t gdn_prefill_workspace_bytes(const gdn_shape_t *shape);
  * device) would stall the work queued on its other streams.
  *
  * The scratch is one static device array of GDN_PREFILL_STATIC_SCRATCH_BYTES
- * per device, reserved when the library's module loads; its address is looked
- * up once per device.  The call allocates and frees nothing.  A shape whose
+ * per device, reserved when the library's module loads in the device's context
+ * (with lazy module loading, at the first call on that device).  The first call
+ * on a device, and the first after its context was destroyed and made again
+ * (cudaDeviceReset), looks up the array's device address and keeps it with the
+ * context; make that first call before any stream capture.  The call allocates
+ * and frees nothing.  A shape whose
  * gdn_prefill_workspace_bytes exceeds the scratch returns GDN_ERR_WORKSPACE
  * before anything is queued (one sequence of 32 heads fits 480 tokens).
  * Nothing in the scratch has to start at zero: the first kernel writes every

@@ -1,7 +1,9 @@
 // C ABI of the KDA / Gated DeltaNet step: argument validation and dispatch.
 // Every check runs on the host before anything is queued; nothing here
 // allocates, copies or synchronises.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "gdn.h"
@@ -111,21 +113,48 @@ bool plan_for(const gdn_shape_t *s, gdn::StepPlan *plan)
 }
 
 // Scratch of gdn_prefill_chunked_static, for callers that cannot allocate:
-// a module-scope device array, reserved when the module loads.  Its device
-// address is looked up once per device; writers race benignly (same value).
+// a module-scope device array, reserved when the module loads in a context.
+// Its device address is looked up once per device and context: a context torn
+// down and made again (cudaDeviceReset) reloads the module at a new address,
+// so the cached address is kept together with the context it belongs to.
+// Writers race benignly (every writer stores the same pair).
 static __device__ __align__(256) unsigned char g_prefill_scratch[GDN_PREFILL_STATIC_SCRATCH_BYTES];
-void *g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+    CUcontext ctx;
+    void *ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+PFN_cuCtxGetCurrent_v4000 ctx_getter()
+{
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;  // benign race: same value
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }
+    return fn;
+}
 
 void *static_scratch()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
+    PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_getter();
+    if (!get_ctx) return nullptr;
+    ScratchAddr &c = g_scratch_addr[dev];
+    CUcontext ctx = nullptr;  // NULL until the runtime has made a context current
+    if (get_ctx(&ctx) == CUDA_SUCCESS && ctx && c.ctx == ctx && c.ptr) return c.ptr;
+    void *p = nullptr;  // the lookup makes the device's primary context current if needed
+    if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
+    c.ptr = p;
+    c.ctx = ctx;
+    return p;
 }
 
 gdn_status_t run_step(const gdn_shape_t *s, const gdn::StepArgs &a, cudaStream_t stream)

@@ -69,6 +69,19 @@ __device__ __forceinline__ uint64_t op_desc_sw128(uint32_t base, int k0)
     return d;
 }
 
+// Byte offset of 16-bit element (r, k) of a K-major operand with `rows` rows in the
+// 128-byte swizzled layout (1024-byte aligned base): K splits into atoms of 64
+// elements, atom a holding every row at a * rows * 128; inside an atom rows are
+// 128 bytes, 8-row groups 1024 bytes apart, and the 16-byte chunk c of row r sits
+// at chunk position c ^ (r % 8) -- the layout a TMA box with
+// CU_TENSOR_MAP_SWIZZLE_128B writes, and what op_desc_sw128 describes.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int r, int k, int rows)
+{
+    const int kk = k & 63;
+    return static_cast<uint32_t>((k >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                 ((((kk >> 3) ^ (r & 7)) & 7) << 4) + (kk & 7) * 2);
+}
+
 // Instruction descriptor of kind::f16: fp16 (or bf16) A and B, fp32 D, both K-major.
 __host__ __device__ __forceinline__ uint32_t idesc_f16(int M, int N, bool negate_a, bool bf16 = false)
 {
@@ -110,6 +123,19 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
+
+// D[tmem] (+)= A * B^T with A in TMEM: row m of A in lane m, its 16-bit K values two
+// to a 32-bit column (K-step k0 at column k0 / 2); B from shared memory.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
         : "memory");
 }
 
@@ -171,6 +197,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
         "r"(__float_as_uint(v[15]))
         : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns, raw words (no wait).
+__device__ __forceinline__ void tmem_st16u_nowait(uint32_t taddr, const uint32_t (&w)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&w)[16])
+{
+    tmem_st16u_nowait(taddr, w);
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 

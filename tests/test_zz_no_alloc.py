@@ -48,11 +48,14 @@ def test_scratch_limit_is_checked_before_anything_is_queued():
                                           None) == gdn.GDN_ERR_SHAPE
 
 
-def _run(shape, seed, static):
+def _upload(shape, seed):
     params = synth.make_params(shape, seed=seed, slow_decay=True)
     inp = synth.make_inputs(shape, seed=seed, slow_decay=True)
     state = synth.make_state(shape, seed=seed)
-    case = dev.upload(shape, params, inp, state)
+    return dev.upload(shape, params, inp, state)
+
+
+def _call(case, static):
     sh = case.abi_shape()
     st = torch.cuda.current_stream().cuda_stream
     if static:
@@ -72,9 +75,14 @@ def test_two_static_calls_in_a_row_match_the_workspace_entry_point():
     second = synth.Shape(B=3, T=61, H_qk=2, H_v=4, d_k=128, d_v=128, kda=True, lb_gate=True)
     assert gdn.gdn_kernel_variant(_abi(first), gdn.OP_PREFILL) == "kda_chunked<16>"
     runs = [(first, 50), (second, 51)]
-    statics = [_run(s, seed, True) for s, seed in runs]       # two calls in a row
-    for (s, seed), a in zip(runs, statics):
-        b = _run(s, seed, False)
+    cases = [_upload(s, seed) for s, seed in runs]
+    torch.cuda.synchronize()
+    _call(cases[0], True)                  # the first call may load the module
+    free_before = torch.cuda.mem_get_info()[0]
+    _call(cases[1], True)                  # the second call in a row
+    assert torch.cuda.mem_get_info()[0] == free_before, "the static call allocated device memory"
+    for (s, seed), a in zip(runs, cases):
+        b = _call(_upload(s, seed), False)
         assert torch.equal(a.out, b.out), f"out differs for {s}"
         assert torch.equal(a.state, b.state), f"state differs for {s}"
         assert torch.equal(a.conv_state, b.conv_state), f"conv_state differs for {s}"
