@@ -365,9 +365,9 @@ gdn_status_t gdn_device_status(void)
 {
     const unsigned int e = gdn::take_stream_error(), p = gdn::take_prefill_error(),
                        q = gdn::take_step_error(), r = gdn::take_kda_prefill_error(),
-                       w = gdn::take_proj_error();
-    if (e == ~0u || p == ~0u || q == ~0u || r == ~0u || w == ~0u) return GDN_ERR_CUDA;
-    return (e | p | q | r | w) ? GDN_ERR_TIMEOUT : GDN_OK;
+                       w = gdn::take_proj_error(), c = gdn::take_c64_error();
+    if (e == ~0u || p == ~0u || q == ~0u || r == ~0u || w == ~0u || c == ~0u) return GDN_ERR_CUDA;
+    return (e | p | q | r | w | c) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 const char *gdn_kernel_variant(const gdn_shape_t *s, int op)

@@ -567,7 +567,10 @@ bool chunked_eligible(const gdn_shape_t &s, const StepArgs &a)
 }
 
 // Shapes that run the two-kernel chunked form over a workspace.
-bool two_stage_shape(const gdn_shape_t &s) { return !chunked_shape(s) && kda_chunk_shape(s); }
+bool two_stage_shape(const gdn_shape_t &s)
+{
+    return !chunked_shape(s) && !c64_shape(s) && kda_chunk_shape(s);
+}
 
 cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
 {
@@ -627,6 +630,7 @@ size_t prefill_workspace_bytes(const gdn_shape_t &s)
 const char *prefill_variant(const gdn_shape_t &s, int num_sms)
 {
     if (chunked_shape(s)) return "chunked<128,32>";
+    if (c64_shape(s)) return "chunked<128,64>";
     if (two_stage_shape(s)) return "kda_chunked<16>";
     StepPlan plan;
     const int sms = num_sms > 0 ? num_sms : 148;
@@ -638,6 +642,10 @@ const char *prefill_variant(const gdn_shape_t &s, int num_sms)
 gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspace, int num_sms,
                          cudaStream_t stream)
 {
+    if (c64_shape(s) && c64_pointers_ok(a)) {
+        cudaError_t e = launch_c64(a, stream);
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
     if (chunked_eligible(s, a)) {
         cudaError_t e = launch_chunked(a, stream);
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

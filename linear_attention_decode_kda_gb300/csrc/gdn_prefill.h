@@ -32,4 +32,12 @@ size_t kda_chunk_workspace_bytes(const gdn_shape_t &s);
 cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t stream);
 unsigned int take_kda_prefill_error();
 
+// 64-token chunked form on tcgen05 (gdn_c64_prefill.cu): per-head decay, d = 128, bf16 rows,
+// shape->chunk == 64; no workspace.
+bool c64_shape(const gdn_shape_t &s);
+// Its pointer rule beyond the ABI's: qkv and z 16-byte aligned (they arrive by TMA).
+bool c64_pointers_ok(const StepArgs &a);
+cudaError_t launch_c64(const StepArgs &a, cudaStream_t stream);
+unsigned int take_c64_error();
+
 }  // namespace gdn

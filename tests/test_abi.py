@@ -147,15 +147,22 @@ def test_gate_variants_are_accepted(lib):
 
 
 def test_prefill_routing_and_workspace(lib):
-    """Per-head decay, bf16 rows, d = 128, chunk 32: the single tensor-core kernel,
-    no workspace.  Other chunks, per-channel decay or fp32 rows at d = 128 and
-    T > 4: the two-kernel form, one 34,304-byte block per (sequence, head,
-    16-token chunk).  Otherwise the recurrent kernel, no workspace."""
+    """Per-head decay, bf16 rows, d = 128: chunk 64 runs the 64-token tensor-core
+    kernel and chunk 32 the 32-token one, neither with a workspace (at any T).
+    Other chunks, per-channel decay or fp32 rows at d = 128 and T > 4: the
+    two-kernel form, one 34,304-byte block per (sequence, head, 16-token chunk).
+    Otherwise the recurrent kernel, no workspace."""
     s = _shape(T=100, kda=False)
     s.chunk = 32
     assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "chunked<128,32>"
     assert gdn.gdn_prefill_workspace_bytes(s) == 0
     s.chunk = 64
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "chunked<128,64>"
+    assert gdn.gdn_prefill_workspace_bytes(s) == 0
+    s.T = 3
+    assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "chunked<128,64>"
+    s.T = 100
+    s.chunk = 16
     assert gdn.gdn_kernel_variant(s, gdn.OP_PREFILL) == "kda_chunked<16>"
     assert gdn.gdn_prefill_workspace_bytes(s) == 2 * 4 * 7 * 34304
     s = _shape(T=100)

@@ -70,9 +70,12 @@ def test_verify_gate_variants_bitwise_equal_decode(B):
     # chunked tensor-core prefill with the sigmoid output gate (GDN gate)
     (synth.Shape(B=2, T=200, H_qk=2, H_v=4, d_k=128, d_v=128, kda=False, sigmoid_out=True,
                  chunk=32), PREFILL_TOL, "chunked<128,32>"),
-    # and on the two-kernel form
+    # the 64-token tensor-core kernel
     (synth.Shape(B=2, T=200, H_qk=2, H_v=4, d_k=128, d_v=128, kda=False, sigmoid_out=True),
-     DECODE_TOL, "kda_chunked<16>"),
+     PREFILL_TOL, "chunked<128,64>"),
+    # and the two-kernel form
+    (synth.Shape(B=2, T=200, H_qk=2, H_v=4, d_k=128, d_v=128, kda=False, sigmoid_out=True,
+                 chunk=16), DECODE_TOL, "kda_chunked<16>"),
     # the bounded per-channel gate on the two-kernel chunked form
     (synth.Shape(B=2, T=70, H_qk=2, H_v=4, d_k=128, d_v=128, kda=True, lb_gate=True,
                  sigmoid_out=True), DECODE_TOL, "kda_chunked<16>"),

@@ -200,10 +200,12 @@ def _prefill(shape, seed=0, slow=False, tol=PREFILL_TOL, bf16_out=False, variant
 
 @pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 200])
 def test_prefill_ragged_lengths(T):
-    """The single tensor-core kernel (chunk 32), and the two-kernel form (chunk 64)."""
+    """The 32-token and the 64-token tensor-core kernels (chunk 32, 64), and the
+    two-kernel form (chunk 16)."""
     shape = synth.Shape(B=2, T=T, H_qk=4, H_v=8, d_k=128, d_v=128, kda=False, chunk=32)
     _prefill(shape, slow=True, variant="chunked<128,32>")
-    _prefill(dataclasses.replace(shape, chunk=64), slow=True,
+    _prefill(dataclasses.replace(shape, chunk=64), slow=True, variant="chunked<128,64>")
+    _prefill(dataclasses.replace(shape, chunk=16), slow=True,
              variant="kda_chunked<16>" if T > 4 else None)
 
 
@@ -213,7 +215,8 @@ def test_prefill_chunked_head_groups(H_qk, H_v):
     shape = synth.Shape(B=3, T=130, H_qk=H_qk, H_v=H_v, d_k=128, d_v=128, kda=False, chunk=32)
     _prefill(shape, seed=5, variant="chunked<128,32>")
     _prefill(shape, seed=6, slow=True)
-    _prefill(dataclasses.replace(shape, chunk=64), seed=6, slow=True, variant="kda_chunked<16>")
+    _prefill(dataclasses.replace(shape, chunk=64), seed=6, slow=True, variant="chunked<128,64>")
+    _prefill(dataclasses.replace(shape, chunk=16), seed=6, slow=True, variant="kda_chunked<16>")
 
 
 def test_prefill_chunked_bf16_out():
@@ -227,7 +230,9 @@ def test_prefill_kda_slow_decay():
 
 
 def test_prefill_gdn_b4_t4096():
-    _prefill(synth.WORKLOADS["gdn_prefill_b4_t4096"]["shape"])
+    """The full-size GDN prefill in the launch the bench times, every output and final
+    state against the oracle's 4096 sequential steps."""
+    _prefill(synth.WORKLOADS["gdn_prefill_b4_t4096"]["shape"], variant="chunked<128,64>")
 
 
 def test_stream_shape_with_unaligned_scalars_falls_back_and_matches():
