@@ -58,17 +58,19 @@ using namespace dev;
 constexpr int D = 128;       // d_k = d_v
 constexpr int CK = 64;       // chunk length
 constexpr int NT = 512;      // threads: 16 warps
-constexpr int NCONV = 384;   // conv threads (warps 0-11)
+constexpr int NCONV = 384;   // q, k, v channels of one value head
 constexpr int RAWR = CK + 3; // input rows a chunk reads: its 64 and the 3 before
 
-// Dynamic shared memory (bytes from a 1024-byte aligned base).
-// [K; Q]: rows 0-63 K, 64-127 Q, 128-byte swizzled K-major (two atoms of 64 channels).
-constexpr uint32_t S_KQH = 0, S_KQL = 32768;
-// K^T and V^T: [128 channels][64 tokens] canonical K-major with 8-row groups 1040
-// bytes apart (16 bytes of padding spread the conv threads' stores over the banks).
-constexpr uint32_t TSBO = 1040;
-constexpr uint32_t T_BYTES = 16 * TSBO;
-constexpr uint32_t S_KTH = 65536, S_KTL = S_KTH + T_BYTES, S_VTH = S_KTL + T_BYTES,
+// Dynamic shared memory (bytes from a 1024-byte aligned base).  Operands are K-major
+// in the canonical no-swizzle layout: 8 x 16-byte core matrices, LBO bytes between
+// neighbours along K, SBO bytes between 8-row groups.
+// [K; Q]: rows 0-63 K, 64-127 Q, 128 channels; LBO 144 spreads the conv threads'
+// stores of one token row over all banks.
+constexpr uint32_t QLBO = 144, QSBO = 16 * QLBO, Q_BYTES = 16 * QSBO;
+constexpr uint32_t S_KQH = 0, S_KQL = Q_BYTES;
+// K^T and V^T: [128 channels][64 tokens]; SBO 1040 spreads the stores of 8-token rows.
+constexpr uint32_t TSBO = 1040, T_BYTES = 16 * TSBO;
+constexpr uint32_t S_KTH = 2 * Q_BYTES, S_KTL = S_KTH + T_BYTES, S_VTH = S_KTL + T_BYTES,
                    S_VTL = S_VTH + T_BYTES;
 constexpr uint32_t S_RAW = ((S_VTL + T_BYTES + 1023) / 1024) * 1024;  // q, k, v boxes [67][128] bf16
 constexpr uint32_t RAW_BOX = RAWR * D * 2;
@@ -76,44 +78,44 @@ constexpr uint32_t S_Z = ((S_RAW + 3 * RAW_BOX + 1023) / 1024) * 1024;  // z box
 constexpr uint32_t S_WIN = S_Z + CK * D * 2;                            // fp32 window [3][384]
 constexpr uint32_t SMEM_USED = S_WIN + 3 * NCONV * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
-static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+static_assert(SMEM_BYTES + 4096 <= 232448, "shared memory per block");
 // Reused regions.  The K rows of [K; Q] are dead after the Gram product: they take
-// T1, T2 (canonical [64][64], 8 KB each), then W (swizzled [64][128], two atoms).
-constexpr uint32_t KP0 = S_KQH, KP1 = S_KQH + 16384, KP2 = S_KQL, KP3 = S_KQL + 16384;
-// M (canonical [64][64]) takes V^T's place after the U product.
+// T1 and T2 ([64][64], SBO 1024, 8 KB each), then W (the [W; Q] operand of the S0 product).
+constexpr uint32_t S_T1H = S_KQH, S_T2H = S_KQH + 8192, S_T1L = S_KQL, S_T2L = S_KQL + 8192;
+static_assert(8192 + 8192 <= 8 * QSBO, "T1 and T2 inside the K rows");
+// M ([64][64], SBO 1024) takes V^T's place after the U product.
 constexpr uint32_t S_MH = S_VTH, S_ML = S_VTH + 8192;
-// V_new and V_new diag(d) (canonical [128][64], 16 KB each) take [K; Q] after the S0 products.
-constexpr uint32_t S_VNH = S_KQH, S_VNL = S_KQH + 16384, S_VDH = S_KQL, S_VDL = S_KQL + 16384;
-// fp32 scratch of the inverse inside the raw-row region (free between the conv and
-// the next chunk's copy): A and T [64][65], the block products [3][16][17].
-constexpr int FS = CK + 1;
-constexpr uint32_t S_AF = S_RAW, S_TF = S_AF + CK * FS * 4, S_RF = S_TF + CK * FS * 4;
-static_assert(S_RF + 3 * 16 * 17 * 4 <= S_RAW + 3 * RAW_BOX, "inverse scratch");
 static_assert(S_ML + 8192 <= S_VTH + T_BYTES, "M operand");
+// fp32 scratch of the inverse inside the raw-row region (free between the conv and
+// the next chunk's copy): A and T [64][68], the block products [3][16][20] (rows
+// 16-byte aligned for 128-bit loads).
+constexpr int FS = CK + 4, RS = 20;
+constexpr uint32_t S_AF = S_RAW, S_TF = S_AF + CK * FS * 4, S_RF = S_TF + CK * FS * 4;
+static_assert(S_RF + 3 * 16 * RS * 4 <= S_RAW + 3 * RAW_BOX, "inverse scratch");
 
 // TMEM columns.
 constexpr uint32_t TM_S = 0;     // 128: S^T fp32
-constexpr uint32_t TM_SH = 128;  // 64: S^T fp16 hi, two to a column
-constexpr uint32_t TM_SL = 192;  // 64: S^T fp16 lo
-constexpr uint32_t TM_G = 256;   // 64: Gram, then S0^T Q^T
-constexpr uint32_t TM_W = 320;   // 64: W^T
-constexpr uint32_t TM_U = 384;   // 64: U^T, then V_new^T
-constexpr uint32_t TM_OV = 448;  // 64: V_new^T M^T
+constexpr uint32_t TM_SH = 128;  // 64: S0^T fp16 hi, two to a column (A of the S0 product) ...
+constexpr uint32_t TM_SL = 192;  // 64: ... and lo; after that product:
+constexpr uint32_t TM_VNH = 128, TM_VNL = 160, TM_VDH = 192, TM_VDL = 224;  // V_new, V_new diag(d)
+constexpr uint32_t TM_X1 = 256;  // 64: W^T, then V_new^T M^T (OV)
+constexpr uint32_t TM_U = 320;   // 64: U^T
+constexpr uint32_t TM_X3 = 384;  // 64: Gram, then S0^T W^T (PW)
+constexpr uint32_t TM_PQ = 448;  // 64: S0^T Q^T (written with PW as one N = 128 product)
 
 __device__ unsigned int g_c64_error;  // bit 0: a bounded mbarrier wait gave up
 
 struct C64Shared {
-    float G2[CK];        // cumulative log2-decay inside the chunk
-    float bt[CK];        // beta (0 past the chunk's end)
-    float nq[CK], nk[CK];  // |q|^2, |k|^2 of the raw rows
-    float rk[CK];        // 1 / |k|
-    float rq[CK];        // q_scale / |q|
-    float f1[CK];        // beta_s e^{G_s} rk_s
-    float ds[CK];        // e^{G_last - G_s} rk_s
-    float cq[CK];        // e^{G_t} rq_t
-    float osq[4][CK];    // per TMEM quadrant: partial sums of o^2
+    float G2[CK];          // cumulative log2-decay inside the chunk
+    float bt[CK];          // beta (0 past the chunk's end)
+    float nqp[2][CK], nkp[2][CK];  // |q|^2, |k|^2 of the raw rows, per half of the channels
+    float rk[CK];          // 1 / |k|
+    float rq[CK];          // q_scale / |q|
+    float f1[CK];          // beta_s e^{G_s} rk_s
+    float ds[CK];          // e^{G_last - G_s} rk_s
+    float cq[2][CK];       // e^{G_t} rq_t, by chunk parity
+    float osq[4][CK];      // per TMEM quadrant: partial sums of o^2
     float rinv[CK];
-    float egl;           // e^{G_last}
     uint64_t raw_full, z_full, mma_bar;
     uint32_t tmem;
 };
@@ -177,11 +179,10 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-// Byte offset of element (r, k) of a canonical K-major operand whose 8-row groups
-// are `sbo` bytes apart (16-byte core-matrix rows, K groups 128 bytes apart).
-__device__ __forceinline__ uint32_t cano(int r, int k, uint32_t sbo)
+// Byte offset of element (r, k) of a canonical K-major operand.
+__device__ __forceinline__ uint32_t cano(int r, int k, uint32_t lbo, uint32_t sbo)
 {
-    return static_cast<uint32_t>(r >> 3) * sbo + static_cast<uint32_t>(k >> 3) * 128 +
+    return static_cast<uint32_t>(r >> 3) * sbo + static_cast<uint32_t>(k >> 3) * lbo +
            static_cast<uint32_t>(r & 7) * 16 + static_cast<uint32_t>(k & 7) * 2;
 }
 
@@ -197,31 +198,41 @@ __device__ __forceinline__ void put8(unsigned char *hi, unsigned char *lo, uint3
     *reinterpret_cast<uint4 *>(lo + off) = l;
 }
 
-// Writes the fp16 hi / lo copy of S^T columns i0 .. i0 + 31 of this thread's lane.
-__device__ __forceinline__ void put_s16(uint32_t tm, int lb, int i0, const float (&s)[32])
+__device__ __forceinline__ void tmem_st8u_nowait(uint32_t taddr, const uint32_t (&w)[8])
 {
-    uint32_t h[16], l[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) split2(s[2 * k], s[2 * k + 1], h[k], l[k]);
-    tc::tmem_st16u_nowait(tc::taddr(tm, lb, TM_SH + i0 / 2), h);
-    tc::tmem_st16u_nowait(tc::taddr(tm, lb, TM_SL + i0 / 2), l);
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
-__device__ __forceinline__ uint64_t cdesc(uint32_t base, int k0, uint32_t sbo)
+// Descriptor of the K step at column k0 of a canonical operand.
+__device__ __forceinline__ uint64_t cdesc(uint32_t base, int k0, uint32_t lbo, uint32_t sbo)
 {
-    return tc::op_desc_strided(base + static_cast<uint32_t>(k0 >> 3) * 128, 128, sbo);
+    return tc::op_desc_strided(base + static_cast<uint32_t>(k0 >> 3) * lbo, lbo, sbo);
 }
 
-// D (+)= (A_hi + A_lo)(B_hi + B_lo)^T without lo*lo, both operands canonical K-major.
+// D (+)= (A_hi + A_lo)(B_hi + B_lo)^T without lo*lo, both operands canonical in shared memory.
 __device__ __forceinline__ void mma3c(uint32_t d, uint32_t ah, uint32_t al, uint32_t asbo, uint32_t bh,
                                       uint32_t bl, uint32_t bsbo, int kdim, uint32_t idesc, bool acc)
 {
     for (int k0 = 0; k0 < kdim; k0 += 16) {
-        const uint64_t dah = cdesc(ah, k0, asbo), dal = cdesc(al, k0, asbo);
-        const uint64_t dbh = cdesc(bh, k0, bsbo), dbl = cdesc(bl, k0, bsbo);
+        const uint64_t dah = cdesc(ah, k0, 128, asbo), dal = cdesc(al, k0, 128, asbo);
+        const uint64_t dbh = cdesc(bh, k0, 128, bsbo), dbl = cdesc(bl, k0, 128, bsbo);
         tc::mma_f16(d, dah, dbh, idesc, acc || k0 > 0);
         tc::mma_f16(d, dah, dbl, idesc, true);
         tc::mma_f16(d, dal, dbh, idesc, true);
+    }
+}
+
+// The same with A in TMEM (hi at column ah, lo at al; K step k0 at column + k0 / 2).
+__device__ __forceinline__ void mma3t(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl,
+                                      uint32_t blbo, uint32_t bsbo, int kdim, uint32_t idesc, bool acc)
+{
+    for (int k0 = 0; k0 < kdim; k0 += 16) {
+        const uint64_t dbh = cdesc(bh, k0, blbo, bsbo), dbl = cdesc(bl, k0, blbo, bsbo);
+        tc::mma_f16_ta(d, ah + k0 / 2, dbh, idesc, acc || k0 > 0);
+        tc::mma_f16_ta(d, ah + k0 / 2, dbl, idesc, true);
+        tc::mma_f16_ta(d, al + k0 / 2, dbh, idesc, true);
     }
 }
 
@@ -232,10 +243,8 @@ __device__ __forceinline__ void publish()
     __syncthreads();
 }
 
-__device__ __forceinline__ void bar_epi()  // warps 12-15
-{
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
+__device__ __forceinline__ void bar_a() { asm volatile("bar.sync 1, 256;" ::: "memory"); }  // warps 0-7
+__device__ __forceinline__ void bar_b() { asm volatile("bar.sync 2, 256;" ::: "memory"); }  // warps 8-15
 
 __global__ void __launch_bounds__(NT, 1)
 c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
@@ -246,6 +255,7 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
     unsigned char *sm = sm_raw + ((1024u - (tc::smem_u32(sm_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, part = warp >> 2, lb = 32 * quad;
+    const bool grp_a = warp < 8;  // warps 0-7: Gram, A, inverse; 8-15: state copy, output
     const int h = blockIdx.x, b = blockIdx.y, hq = h / a.group;
     const int T = a.T, C = a.C, H = a.H_v;
     const bool clustered = a.group > 1;
@@ -286,39 +296,36 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
 
     // the kept conv window (fp32; the first chunk's 3 earlier rows) and the initial state
     if (tid < NCONV) {
-        const int ten = tid >> 7, c = tid & 127;
-        const int ch = (ten == 0 ? chq : ten == 1 ? chk : chv) + c;
+        const int tn = tid >> 7, c = tid & 127;
+        const int ch = (tn == 0 ? chq : tn == 1 ? chk : chv) + c;
 #pragma unroll
         for (int r = 0; r < 3; ++r) win[r * NCONV + tid] = a.conv_in[(static_cast<size_t>(b) * 3 + r) * C + ch];
     }
-    {   // S[i][j] -> TMEM S^T (lane j, column i) and its fp16 copy; this warp takes rows 32 part ..
+    {   // S[i][j] -> TMEM S^T (lane j, column i); this warp takes rows 32 part .. 32 part + 31
         const float *Sg = a.state_in + head * D * D;
-        float s[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = Sg[(32 * part + k) * D + lb + lane];
-        uint32_t w[16];
+        for (int q = 0; q < 2; ++q) {
+            uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(s[k]);
-        tc::tmem_st16u_nowait(tc::taddr(tm, lb, TM_S + 32 * part), w);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(s[16 + k]);
-        tc::tmem_st16u_nowait(tc::taddr(tm, lb, TM_S + 32 * part + 16), w);
-        put_s16(tm, lb, 32 * part, s);
+            for (int k = 0; k < 16; ++k) w[k] = __float_as_uint(Sg[(32 * part + 16 * q + k) * D + lb + lane]);
+            tc::tmem_st16u_nowait(tc::taddr(tm, lb, TM_S + 32 * part + 16 * q), w);
+        }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
     if (clustered) cluster_arrive_relaxed();  // this CTA has read the shared q/k window
 
-    // conv threads: tensor ten (0 q, 1 k, 2 v), channels 4 lane .. 4 lane + 3, token
-    // blocks 2 (warp % 4) and 2 (warp % 4) + 1 of every chunk
-    const int ten = warp >> 2;
-    float4 cw[4];
-    if (warp < 12) {
-        const int ch0 = (ten == 0 ? chq : ten == 1 ? chk : chv) + 4 * lane;
+    // conv: every warp takes tokens 8 tb .. 8 tb + 7 and channels 64 hf + 2 lane, + 1
+    // of q, k and v
+    const int hf = (warp >> 3) & 1, tb = warp & 7;
+    float4 cw[3][2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) cw[c] = reinterpret_cast<const float4 *>(a.conv_w)[ch0 + c];
+    for (int tn = 0; tn < 3; ++tn) {
+        const int ch0 = (tn == 0 ? chq : tn == 1 ? chk : chv) + 64 * hf + 2 * lane;
+        cw[tn][0] = reinterpret_cast<const float4 *>(a.conv_w)[ch0];
+        cw[tn][1] = reinterpret_cast<const float4 *>(a.conv_w)[ch0 + 1];
     }
 
-    // gate logits of the next chunk: warp 12, tokens 2 lane and 2 lane + 1
+    // gate logits of the next chunk: warp 15, tokens 2 lane and 2 lane + 1
     const float A_h = expf(a.A_log[h]);
     const float dt_h = a.dt_bias[h];
     float fx[2] = {0.f, 0.f}, bx[2] = {0.f, 0.f};
@@ -333,63 +340,60 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
             }
         }
     };
-    if (warp == 12) load_gates(0);
+    if (warp == 15) load_gates(0);
     const float nw = a.norm_w[lb + lane];  // output-norm weight of this lane's column
 
     bool ok = true;
     uint32_t mma_ph = 0;
-    auto mma_wait = [&]() {
-        if (ok) ok = mbar_wait_bounded(&ps.mma_bar, mma_ph);
+    auto mma_wait = [&](bool wait) {
+        if (wait && ok) ok = mbar_wait_suspend_bounded(&ps.mma_bar, mma_ph);
         mma_ph ^= 1u;
         tc::fence_after_sync();
     };
     const uint32_t smb = tc::smem_u32(sm);
-    const uint32_t id64 = tc::idesc_f16(128, 64, false), id64n = tc::idesc_f16(128, 64, true),
-                   id128 = tc::idesc_f16(128, 128, false);
+    const uint32_t id64 = tc::idesc_f16(128, 64, false), id128 = tc::idesc_f16(128, 128, false);
 
-    // The output of chunk (cp, np) from TMEM: o = P^T e^{G_t} rq_t + OV^T, the gated
-    // RMSNorm over the 128 columns, y stored.  Warps 12-15 (lane = column j).
+    // The output of chunk (cp, np) from TMEM: o = PQ e^{G_t} rq_t + OV, the gated
+    // RMSNorm over the 128 columns, y stored.  Warps 8-15: lane = column j, tokens
+    // 32 th .. 32 th + 31.
     auto epilogue = [&](int cp, int np, int it) {
-        if (ok) ok = mbar_wait_bounded(&ps.z_full, static_cast<uint32_t>(it & 1));
-        const int j = lb + lane;
+        if (ok) ok = mbar_wait_suspend_bounded(&ps.z_full, static_cast<uint32_t>(it & 1));
+        const int j = lb + lane, th = part & 1;
+        const float *cq = ps.cq[it & 1];
+        float o[32], v[32];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float p16[16], ov16[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_PQ + 32 * th + 16 * q), p16);
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_X1 + 32 * th + 16 * q), ov16);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float x = fmaf(p16[k], cq[32 * th + 16 * q + k], ov16[k]);
+                o[16 * q + k] = x;
+                v[16 * q + k] = x * x;
+            }
+        }
+        ps.osq[quad][32 * th + lane] = reduce_scatter32(v, lane);
+        bar_b();
+        if (tid < 256 + CK) {
+            const int t = tid - 256;
+            const float m = (ps.osq[0][t] + ps.osq[1][t] + ps.osq[2][t] + ps.osq[3][t]) * (1.0f / D);
+            ps.rinv[t] = rsqrtf(m + a.eps_norm);
+        }
+        bar_b();
         const unsigned char *zs = sm + S_Z;
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-            float o[32], v[32];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float p16[16], ov16[16];
-                tc::tmem_ld16(tc::taddr(tm, lb, TM_G + 32 * hf + 16 * q), p16);
-                tc::tmem_ld16(tc::taddr(tm, lb, TM_OV + 32 * hf + 16 * q), ov16);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float x = fmaf(p16[k], ps.cq[32 * hf + 16 * q + k], ov16[k]);
-                    o[16 * q + k] = x;
-                    v[16 * q + k] = x * x;
-                }
-            }
-            const float sq = reduce_scatter32(v, lane);
-            ps.osq[quad][32 * hf + lane] = sq;
-            bar_epi();
-            if (warp == 12) {
-                const int t = 32 * hf + lane;
-                const float m = (ps.osq[0][t] + ps.osq[1][t] + ps.osq[2][t] + ps.osq[3][t]) * (1.0f / D);
-                ps.rinv[t] = rsqrtf(m + a.eps_norm);
-            }
-            bar_epi();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int t = 32 * hf + k;
-                if (t < np) {
-                    const float zz = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(zs + (t * D + j) * 2));
-                    const float gz = a.sig_gate ? sigmoid_fast(zz) : silu_fast(zz);
-                    const float y = o[k] * ps.rinv[t] * nw * gz;
-                    const size_t idx = ((static_cast<size_t>(b) * T + cp + t) * H + h) * D + j;
-                    if (a.out_bf16)
-                        reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
-                    else
-                        reinterpret_cast<float *>(a.out)[idx] = y;
-                }
+        for (int k = 0; k < 32; ++k) {
+            const int t = 32 * th + k;
+            if (t < np) {
+                const float zz = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(zs + (t * D + j) * 2));
+                const float gz = a.sig_gate ? sigmoid_fast(zz) : silu_fast(zz);
+                const float y = o[k] * ps.rinv[t] * nw * gz;
+                const size_t idx = ((static_cast<size_t>(b) * T + cp + t) * H + h) * D + j;
+                if (a.out_bf16)
+                    reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
+                else
+                    reinterpret_cast<float *>(a.out)[idx] = y;
             }
         }
         fence_proxy_async_smem();  // the z stage is read: the next copy may land there
@@ -400,266 +404,286 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
     for (int c0 = 0, it = 0; c0 < T; c0 += CK, ++it) {
         const int n = min(CK, T - c0);
 
-        if (warp < 12) {
-            // ---- conv + SiLU of two 8-token blocks; q -> Q rows, k -> K rows and K^T, v -> V^T
-            if (ok) ok = mbar_wait_bounded(&ps.raw_full, static_cast<uint32_t>(it & 1));
-            const unsigned char *raw = sm + S_RAW + ten * RAW_BOX;
-#pragma unroll 1
-            for (int blk = 0; blk < 2; ++blk) {
-                const int tb = 2 * quad + blk;  // token block: tokens 8 tb .. 8 tb + 7
-                float xw[3][4];
+        // ---- gates of this chunk (warp 15)
+        if (warp == 15) {
+            float g[2], bb[2];
 #pragma unroll
-                for (int r = 0; r < 3; ++r) {
-                    if (c0 == 0 && tb == 0) {
+            for (int u = 0; u < 2; ++u) {
+                const bool in = 2 * lane + u < n;
+                g[u] = in ? -A_h * softplus_fast(fx[u] + dt_h) : 0.f;
+                bb[u] = in ? sigmoid_fast(bx[u]) : 0.f;
+            }
+            if (c0 + CK < T) load_gates(c0 + CK);
+            float sc = g[0] + g[1];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) xw[r][c] = win[r * NCONV + ten * 128 + 4 * lane + c];
-                    } else {
-                        const uint2 u = *reinterpret_cast<const uint2 *>(raw + ((8 * tb + r) * D + 4 * lane) * 2);
-                        xw[r][0] = __uint_as_float(u.x << 16);
-                        xw[r][1] = __uint_as_float(u.x & 0xffff0000u);
-                        xw[r][2] = __uint_as_float(u.y << 16);
-                        xw[r][3] = __uint_as_float(u.y & 0xffff0000u);
-                    }
-                }
-                uint32_t hn[8][2], ln[8][2];
-                float nrm[8];
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sc, off);
+                if (lane >= off) sc += y;
+            }
+            ps.G2[2 * lane] = (sc - g[1]) * kLog2e;
+            ps.G2[2 * lane + 1] = sc * kLog2e;
+            ps.bt[2 * lane] = bb[0];
+            ps.bt[2 * lane + 1] = bb[1];
+        }
+
+        // ---- conv + SiLU: q -> Q rows, k -> K rows and K^T, v -> V^T (all warps)
+        if (ok) ok = mbar_wait_suspend_bounded(&ps.raw_full, static_cast<uint32_t>(it & 1));
 #pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int t = 8 * tb + rr;
-                    const uint2 u = *reinterpret_cast<const uint2 *>(raw + ((t + 3) * D + 4 * lane) * 2);
-                    float x[4];
-                    x[0] = __uint_as_float(u.x << 16);
-                    x[1] = __uint_as_float(u.x & 0xffff0000u);
-                    x[2] = __uint_as_float(u.y << 16);
-                    x[3] = __uint_as_float(u.y & 0xffff0000u);
-                    float y[4];
+        for (int tn = 0; tn < 3; ++tn) {
+            const unsigned char *raw = sm + S_RAW + tn * RAW_BOX;
+            const int cl = 64 * hf + 2 * lane;  // first of this lane's two channels in the tensor
+            float xw[3][2];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float acc = cw[c].x * xw[0][c];
-                        acc = fmaf(cw[c].y, xw[1][c], acc);
-                        acc = fmaf(cw[c].z, xw[2][c], acc);
-                        acc = fmaf(cw[c].w, x[c], acc);
-                        y[c] = t < n ? silu_fast(acc) : 0.f;
-                        xw[0][c] = xw[1][c];
-                        xw[1][c] = xw[2][c];
-                        xw[2][c] = x[c];
-                    }
-                    nrm[rr] = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
-                    split2(y[0], y[1], hn[rr][0], ln[rr][0]);
-                    split2(y[2], y[3], hn[rr][1], ln[rr][1]);
-                    if (ten < 2) {  // row t (k) or 64 + t (q) of [K; Q], 4 channels = 8 bytes
-                        const int R = ten == 0 ? 64 + t : t;
-                        const uint32_t off = (lane >> 4) * 16384 + (R >> 3) * 1024 + (R & 7) * 128 +
-                                             (((((lane & 15) >> 1) ^ (R & 7)) & 7) << 4) + (lane & 1) * 8;
-                        *reinterpret_cast<uint2 *>(sm + S_KQH + off) = make_uint2(hn[rr][0], hn[rr][1]);
-                        *reinterpret_cast<uint2 *>(sm + S_KQL + off) = make_uint2(ln[rr][0], ln[rr][1]);
-                    }
-                }
-                if (ten >= 1) {  // K^T / V^T rows 4 lane + c: the block's 8 tokens, 16 bytes
-                    unsigned char *th = sm + (ten == 1 ? S_KTH : S_VTH);
-                    unsigned char *tl = sm + (ten == 1 ? S_KTL : S_VTL);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
-                        uint4 vh, vl;
-                        vh.x = __byte_perm(hn[0][c >> 1], hn[1][c >> 1], sel);
-                        vh.y = __byte_perm(hn[2][c >> 1], hn[3][c >> 1], sel);
-                        vh.z = __byte_perm(hn[4][c >> 1], hn[5][c >> 1], sel);
-                        vh.w = __byte_perm(hn[6][c >> 1], hn[7][c >> 1], sel);
-                        vl.x = __byte_perm(ln[0][c >> 1], ln[1][c >> 1], sel);
-                        vl.y = __byte_perm(ln[2][c >> 1], ln[3][c >> 1], sel);
-                        vl.z = __byte_perm(ln[4][c >> 1], ln[5][c >> 1], sel);
-                        vl.w = __byte_perm(ln[6][c >> 1], ln[7][c >> 1], sel);
-                        const uint32_t off = cano(4 * lane + c, 8 * tb, TSBO);
-                        *reinterpret_cast<uint4 *>(th + off) = vh;
-                        *reinterpret_cast<uint4 *>(tl + off) = vl;
-                    }
-                }
-                if (ten < 2) {
-                    const float tot = reduce8(nrm, lane);
-                    if ((lane & 3) == 0) {
-                        const int t = 8 * tb + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-                        (ten == 0 ? ps.nq : ps.nk)[t] = tot;
-                    }
+            for (int r = 0; r < 3; ++r) {
+                if (c0 == 0 && tb == 0) {
+                    xw[r][0] = win[r * NCONV + tn * 128 + cl];
+                    xw[r][1] = win[r * NCONV + tn * 128 + cl + 1];
+                } else {
+                    const uint32_t u = *reinterpret_cast<const uint32_t *>(raw + ((8 * tb + r) * D + cl) * 2);
+                    xw[r][0] = __uint_as_float(u << 16);
+                    xw[r][1] = __uint_as_float(u & 0xffff0000u);
                 }
             }
-        } else {
-            // ---- gates of this chunk (warp 12), then the previous chunk's output and
-            // the fp16 copy of the state it left (warps 12-15)
-            if (warp == 12) {
-                float g[2], bb[2];
+            uint32_t hn[8], ln[8];
+            float nrm[8];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const bool in = 2 * lane + u < n;
-                    g[u] = in ? -A_h * softplus_fast(fx[u] + dt_h) : 0.f;
-                    bb[u] = in ? sigmoid_fast(bx[u]) : 0.f;
+            for (int rr = 0; rr < 8; ++rr) {
+                const int t = 8 * tb + rr;
+                const uint32_t u = *reinterpret_cast<const uint32_t *>(raw + ((t + 3) * D + cl) * 2);
+                const float x0 = __uint_as_float(u << 16), x1 = __uint_as_float(u & 0xffff0000u);
+                float acc0 = cw[tn][0].x * xw[0][0], acc1 = cw[tn][1].x * xw[0][1];
+                acc0 = fmaf(cw[tn][0].y, xw[1][0], acc0);
+                acc1 = fmaf(cw[tn][1].y, xw[1][1], acc1);
+                acc0 = fmaf(cw[tn][0].z, xw[2][0], acc0);
+                acc1 = fmaf(cw[tn][1].z, xw[2][1], acc1);
+                acc0 = fmaf(cw[tn][0].w, x0, acc0);
+                acc1 = fmaf(cw[tn][1].w, x1, acc1);
+                const float y0 = t < n ? silu_fast(acc0) : 0.f, y1 = t < n ? silu_fast(acc1) : 0.f;
+                xw[0][0] = xw[1][0]; xw[1][0] = xw[2][0]; xw[2][0] = x0;
+                xw[0][1] = xw[1][1]; xw[1][1] = xw[2][1]; xw[2][1] = x1;
+                nrm[rr] = y0 * y0 + y1 * y1;
+                split2(y0, y1, hn[rr], ln[rr]);
+                if (tn < 2) {  // row t (k) or 64 + t (q) of [K; Q]
+                    const uint32_t off = cano(tn == 0 ? 64 + t : t, cl, QLBO, QSBO);
+                    *reinterpret_cast<uint32_t *>(sm + S_KQH + off) = hn[rr];
+                    *reinterpret_cast<uint32_t *>(sm + S_KQL + off) = ln[rr];
                 }
-                if (c0 + CK < T) load_gates(c0 + CK);
-                const float pair = g[0] + g[1];
-                float sc = pair;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, sc, off);
-                    if (lane >= off) sc += y;
-                }
-                ps.G2[2 * lane] = (sc - g[1]) * kLog2e;
-                ps.G2[2 * lane + 1] = sc * kLog2e;
-                ps.bt[2 * lane] = bb[0];
-                ps.bt[2 * lane + 1] = bb[1];
             }
-            if (it > 0) {
-#pragma unroll 1
-                for (int i0 = 0; i0 < D; i0 += 32) {
-                    float s[32], s16[16];
-                    tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0), s16);
+            if (tn >= 1) {  // K^T / V^T rows cl, cl + 1: the block's 8 tokens, 16 bytes each
+                unsigned char *th = sm + (tn == 1 ? S_KTH : S_VTH);
+                unsigned char *tl = sm + (tn == 1 ? S_KTL : S_VTL);
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) s[k] = s16[k];
-                    tc::tmem_ld16(tc::taddr(tm, lb, TM_S + i0 + 16), s16);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) s[16 + k] = s16[k];
-                    put_s16(tm, lb, i0, s);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint32_t sel = cc ? 0x7632u : 0x5410u;
+                    const uint4 vh = make_uint4(__byte_perm(hn[0], hn[1], sel), __byte_perm(hn[2], hn[3], sel),
+                                                __byte_perm(hn[4], hn[5], sel), __byte_perm(hn[6], hn[7], sel));
+                    const uint4 vl = make_uint4(__byte_perm(ln[0], ln[1], sel), __byte_perm(ln[2], ln[3], sel),
+                                                __byte_perm(ln[4], ln[5], sel), __byte_perm(ln[6], ln[7], sel));
+                    const uint32_t off = cano(cl + cc, 8 * tb, 128, TSBO);
+                    *reinterpret_cast<uint4 *>(th + off) = vh;
+                    *reinterpret_cast<uint4 *>(tl + off) = vl;
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                epilogue(cp, np, it - 1);
+            }
+            if (tn < 2) {
+                const float tot = reduce8(nrm, lane);
+                if ((lane & 3) == 0) {
+                    const int t = 8 * tb + ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                    (tn == 0 ? ps.nqp : ps.nkp)[hf][t] = tot;
+                }
             }
         }
-        publish();  // B1: conv operands written, previous output read
+        publish();  // B1: the conv operands, the gates and the norms are written
 
-        // ---- Gram product [K; Q] K^T (hi.hi + hi.lo + lo.hi); the z rows of this chunk
-        if (tid == 0) {
-            tc::fence_after_sync();
+        if (grp_a) {
+            // ---- warps 0-7: the Gram product [K; Q] K^T (hi.hi + hi.lo + lo.hi), the
+            // per-token factors, A, and T = (I + A)^-1
+            if (tid == 0) {
+                tc::fence_after_sync();
 #pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t at = (ks >> 2) * 16384;
-                const int k0 = (ks & 3) * 16;
-                const uint64_t ah = tc::op_desc_sw128(smb + S_KQH + at, k0);
-                const uint64_t al = tc::op_desc_sw128(smb + S_KQL + at, k0);
-                tc::mma_f16(tm + TM_G, ah, ah, id64, ks > 0);  // B = rows 0-63 (K) of the same atom
-                tc::mma_f16(tm + TM_G, ah, al, id64, true);
-                tc::mma_f16(tm + TM_G, al, ah, id64, true);
+                for (int k0 = 0; k0 < D; k0 += 16) {
+                    const uint64_t ah = cdesc(smb + S_KQH, k0, QLBO, QSBO), al = cdesc(smb + S_KQL, k0, QLBO, QSBO);
+                    tc::mma_f16(tm + TM_X3, ah, ah, id64, k0 > 0);  // B = rows 0-63 (K)
+                    tc::mma_f16(tm + TM_X3, ah, al, id64, true);
+                    tc::mma_f16(tm + TM_X3, al, ah, id64, true);
+                }
+                tc::mma_commit(&ps.mma_bar);
             }
-            tc::mma_commit(&ps.mma_bar);
+            if (tid < CK) {
+                const int t = tid;
+                const bool in = t < n;
+                const float rk = in ? rsqrtf(ps.nkp[0][t] + ps.nkp[1][t] + a.eps_l2) : 0.f;
+                const float rq = in ? a.q_scale * rsqrtf(ps.nqp[0][t] + ps.nqp[1][t] + a.eps_l2) : 0.f;
+                const float G2t = ps.G2[t], G2l = ps.G2[n - 1];
+                ps.rk[t] = rk;
+                ps.rq[t] = rq;
+                ps.f1[t] = ps.bt[t] * ex2(G2t) * rk;
+                ps.ds[t] = in ? ex2(G2l - G2t) * rk : 0.f;
+                ps.cq[it & 1][t] = ex2(G2t) * rq;
+            }
+            bar_a();
+            mma_wait(true);
+            // A = beta_t rk_t rk_s (k.k) e^{G_t - G_s} (s < t): lanes 0-63 hold the K rows
+            if (quad < 2) {
+                const int t = lb + lane;
+                const float bt = ps.bt[t] * ps.rk[t], G2t = ps.G2[t];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    float v[16];
+                    tc::tmem_ld16(tc::taddr(tm, lb, TM_X3 + 32 * part + 16 * q), v);
+#pragma unroll
+                    for (int k4 = 0; k4 < 16; k4 += 4) {
+                        float e[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int s = 32 * part + 16 * q + k4 + k;
+                            e[k] = (s < t && t < n) ? bt * ps.rk[s] * v[k4 + k] * ex2(G2t - ps.G2[s]) : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(Af + t * FS + 32 * part + 16 * q + k4) = make_float4(e[0], e[1], e[2], e[3]);
+                    }
+                }
+            }
+            bar_a();
+            // four 16 x 16 diagonal blocks by forward substitution (x[m] = 0 for m < c)
+            if (tid < CK) {
+                const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
+                float x[16], ar[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+#pragma unroll
+                    for (int m4 = 0; m4 < r; m4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Af + (o + r) * FS + o + m4);
+                        ar[m4] = a4.x; ar[m4 + 1] = a4.y; ar[m4 + 2] = a4.z; ar[m4 + 3] = a4.w;
+                    }
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int m = 0; m < r; ++m) acc[m & 3] = fmaf(ar[m], x[m], acc[m & 3]);
+                    x[r] = r < c ? 0.f : (r == c ? 1.f : -((acc[0] + acc[1]) + (acc[2] + acc[3])));
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Tf[(o + r) * FS + o + c] = x[r];
+            }
+            bar_a();
+            // the blocks below the diagonal, one block diagonal at a time:
+            // T_ij = -T_ii sum_{m=j}^{i-1} A_im T_mj; a thread takes 4 columns of one row
+#pragma unroll 1
+            for (int dd = 1; dd < 4; ++dd) {
+                const int blk = tid >> 6, i = dd + blk, j = blk, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+                const bool act = blk < 4 - dd;
+                if (act) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int m = j; m < i; ++m)
+#pragma unroll
+                        for (int x4 = 0; x4 < 16; x4 += 4) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(Af + (16 * i + r) * FS + 16 * m + x4);
+                            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                            for (int xx = 0; xx < 4; ++xx) {
+                                const float4 t4 = *reinterpret_cast<const float4 *>(Tf + (16 * m + x4 + xx) * FS + 16 * j + c4);
+                                acc.x = fmaf(av[xx], t4.x, acc.x);
+                                acc.y = fmaf(av[xx], t4.y, acc.y);
+                                acc.z = fmaf(av[xx], t4.z, acc.z);
+                                acc.w = fmaf(av[xx], t4.w, acc.w);
+                            }
+                        }
+                    *reinterpret_cast<float4 *>(Rf + (blk * 16 + r) * RS + c4) = acc;
+                }
+                bar_a();
+                if (act) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int x4 = 0; x4 < 16; x4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Tf + (16 * i + r) * FS + 16 * i + x4);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int xx = 0; xx < 4; ++xx) {
+                            const float4 r4 = *reinterpret_cast<const float4 *>(Rf + (blk * 16 + x4 + xx) * RS + c4);
+                            acc.x = fmaf(av[xx], r4.x, acc.x);
+                            acc.y = fmaf(av[xx], r4.y, acc.y);
+                            acc.z = fmaf(av[xx], r4.z, acc.z);
+                            acc.w = fmaf(av[xx], r4.w, acc.w);
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(Tf + (16 * i + r) * FS + 16 * j + c4) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                }
+                bar_a();
+            }
+        } else {
+            // ---- warps 8-15: the fp16 copy of the state this chunk starts from (A of its
+            // S0 product), the state scaled by e^{G_last} for its update, and the previous
+            // chunk's output
+            mma_wait(false);
+            const float gl = ex2(ps.G2[n - 1]);
+            const int c0s = 64 * (part & 1);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float s[16];
+                tc::tmem_ld16(tc::taddr(tm, lb, TM_S + c0s + 16 * q), s);
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) split2(s[2 * k], s[2 * k + 1], hw[k], lw[k]);
+                tmem_st8u_nowait(tc::taddr(tm, lb, TM_SH + c0s / 2 + 8 * q), hw);
+                tmem_st8u_nowait(tc::taddr(tm, lb, TM_SL + c0s / 2 + 8 * q), lw);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) s[k] *= gl;
+                tc::tmem_st16(tc::taddr(tm, lb, TM_S + c0s + 16 * q), s);
+            }
+            if (it > 0) epilogue(cp, np, it - 1);
+        }
+        publish();  // B2
+        if (tid == 0) {  // the previous output has read the z stage: this chunk's rows
             mbar_expect_tx(&ps.z_full, CK * D * 2);
             tma_load_3d(sm + S_Z, &tm_z, 0, h, b * T + c0, &ps.z_full);
         }
-        // per-token factors of this chunk
-        if (tid < CK) {
-            const int t = tid;
-            const bool in = t < n;
-            const float rk = in ? rsqrtf(ps.nk[t] + a.eps_l2) : 0.f;
-            const float rq = in ? a.q_scale * rsqrtf(ps.nq[t] + a.eps_l2) : 0.f;
-            const float G2t = ps.G2[t], G2l = ps.G2[n - 1];
-            ps.rk[t] = rk;
-            ps.rq[t] = rq;
-            ps.f1[t] = ps.bt[t] * ex2(G2t) * rk;
-            ps.ds[t] = in ? ex2(G2l - G2t) * rk : 0.f;
-            ps.cq[t] = ex2(G2t) * rq;
-            if (t == 0) ps.egl = ex2(G2l);
-        }
-        __syncthreads();
-        mma_wait();
 
-        // ---- A = beta_t rk_t rk_s (k.k) e^{G_t - G_s} (s < t): lanes 0-63 hold K rows
-        if (quad < 2) {
-            const int t = lb + lane;
-            float v[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_G + 16 * part), v);
-            const float bt = ps.bt[t] * ps.rk[t], G2t = ps.G2[t];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int s = 16 * part + k;
-                Af[t * FS + s] = (s < t && t < n) ? bt * ps.rk[s] * v[k] * ex2(G2t - ps.G2[s]) : 0.f;
-            }
-        }
-        __syncthreads();
-
-        // ---- T = (I + A)^-1: four 16 x 16 diagonal blocks by forward substitution,
-        // then the blocks below the diagonal, one block diagonal at a time
-        if (tid < CK) {
-            const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < r; ++m)
-                    if (m >= c) acc = fmaf(Af[(o + r) * FS + o + m], x[m], acc);
-                x[r] = r < c ? 0.f : (r == c ? 1.f : -acc);
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tf[(o + r) * FS + o + c] = x[r];
-        }
-        __syncthreads();
-#pragma unroll 1
-        for (int dd = 1; dd < 4; ++dd) {
-            const int ne = (4 - dd) * 256;
-            for (int e = tid; e < ne; e += NT) {  // R = sum_m A_im T_mj
-                const int blk = e >> 8, i = dd + blk, j = blk, r = (e >> 4) & 15, c = e & 15;
-                float acc = 0.f;
-                for (int m = j; m < i; ++m)
-#pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        acc = fmaf(Af[(16 * i + r) * FS + 16 * m + x], Tf[(16 * m + x) * FS + 16 * j + c], acc);
-                Rf[(blk * 16 + r) * 17 + c] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < ne; e += NT) {  // T_ij = -T_ii R
-                const int blk = e >> 8, i = dd + blk, j = blk, r = (e >> 4) & 15, c = e & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int x = 0; x < 16; ++x) acc = fmaf(Tf[(16 * i + r) * FS + 16 * i + x], Rf[(blk * 16 + x) * 17 + c], acc);
-                Tf[(16 * i + r) * FS + 16 * j + c] = -acc;
-            }
-            __syncthreads();
-        }
-
-        // ---- T1 = T diag(beta e^G rk), T2 = T diag(beta): canonical [64 t][64 s]
+        // ---- T1 = T diag(beta e^G rk), T2 = T diag(beta): [64 t][64 s] into the K rows
         {
             const int t = tid & 63, s0 = 8 * (tid >> 6);
             float v1[8], v2[8];
+            const float4 ta = *reinterpret_cast<const float4 *>(Tf + t * FS + s0);
+            const float4 tb4 = *reinterpret_cast<const float4 *>(Tf + t * FS + s0 + 4);
+            const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb4.x, tb4.y, tb4.z, tb4.w};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int s = s0 + k;
-                const float x = s <= t ? Tf[t * FS + s] : 0.f;
+                const float x = s <= t ? tv[k] : 0.f;
                 v1[k] = x * ps.f1[s];
                 v2[k] = x * ps.bt[s];
             }
-            const uint32_t off = cano(t, s0, 1024);
-            put8(sm + KP0, sm + KP2, off, v1);
-            put8(sm + KP1, sm + KP3, off, v2);
+            const uint32_t off = cano(t, s0, 128, 1024);
+            put8(sm + S_T1H, sm + S_T1L, off, v1);
+            put8(sm + S_T2H, sm + S_T2L, off, v2);
         }
         publish();  // B3
 
         // ---- W^T = K^T T1^T, U^T = V^T T2^T
         if (tid == 0) {
             tc::fence_after_sync();
-            mma3c(tm + TM_W, smb + S_KTH, smb + S_KTL, TSBO, smb + KP0, smb + KP2, 1024, CK, id64, false);
-            mma3c(tm + TM_U, smb + S_VTH, smb + S_VTL, TSBO, smb + KP1, smb + KP3, 1024, CK, id64, false);
+            mma3c(tm + TM_X1, smb + S_KTH, smb + S_KTL, TSBO, smb + S_T1H, smb + S_T1L, 1024, CK, id64, false);
+            mma3c(tm + TM_U, smb + S_VTH, smb + S_VTL, TSBO, smb + S_T2H, smb + S_T2L, 1024, CK, id64, false);
             tc::mma_commit(&ps.mma_bar);
         }
-        mma_wait();
+        mma_wait(true);
         if (tid == 0 && c0 + CK < T) issue_raw(c0 + CK);  // the raw region is free again
 
-        // ---- W operand [t][i] (swizzled, 64 rows) from W^T; M operand [t][s]
+        // ---- W operand: rows 0-63 of [W; Q] from W^T (lane = channel i);
+        // M operand [t][s] from the Gram's Q rows (lanes 64-127)
         {
             const int i = lb + lane;
             float w[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_W + 16 * part), w);
-            unsigned char *wh = sm + (i < 64 ? KP0 : KP1), *wl = sm + (i < 64 ? KP2 : KP3);
-            const int ii = i & 63;
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_X1 + 16 * part), w);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const int t = 16 * part + k;
-                const uint32_t off = (t >> 3) * 1024 + (t & 7) * 128 + ((((ii >> 3) ^ (t & 7)) & 7) << 4) + (ii & 7) * 2;
+                const uint32_t off = cano(16 * part + k, i, QLBO, QSBO);
                 const __half hv = __float2half_rn(w[k]);
-                *reinterpret_cast<__half *>(wh + off) = hv;
-                *reinterpret_cast<__half *>(wl + off) = __float2half_rn(w[k] - __half2float(hv));
+                *reinterpret_cast<__half *>(sm + S_KQH + off) = hv;
+                *reinterpret_cast<__half *>(sm + S_KQL + off) = __float2half_rn(w[k] - __half2float(hv));
             }
         }
         if (quad >= 2) {
             const int t = lb + lane - 64;
             float v[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_G + 16 * part), v);
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_X3 + 16 * part), v);
             const float rq = ps.rq[t], G2t = ps.G2[t];
             float m[16];
 #pragma unroll
@@ -667,72 +691,55 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
                 const int s = 16 * part + k;
                 m[k] = (s <= t && t < n) ? rq * ps.rk[s] * v[k] * ex2(G2t - ps.G2[s]) : 0.f;
             }
-            put8(sm + S_MH, sm + S_ML, cano(t, 16 * part, 1024), m);
-            put8(sm + S_MH, sm + S_ML, cano(t, 16 * part + 8, 1024), m + 8);
+            put8(sm + S_MH, sm + S_ML, cano(t, 16 * part, 128, 1024), m);
+            put8(sm + S_MH, sm + S_ML, cano(t, 16 * part + 8, 128, 1024), m + 8);
         }
         publish();  // B4
 
-        // ---- V_new^T = U^T - S0^T W^T;  P^T = S0^T Q^T   (A = S0^T from TMEM)
+        // ---- [PW | PQ] = S0^T [W; Q]^T, one N = 128 product with A = S0^T from TMEM
         if (tid == 0) {
             tc::fence_after_sync();
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                const int k0 = (ks & 3) * 16;
-                const uint32_t ash = tm + TM_SH + 8 * ks, asl = tm + TM_SL + 8 * ks;
-                const uint64_t wh = tc::op_desc_sw128(smb + ((ks >> 2) ? KP1 : KP0), k0);
-                const uint64_t wl = tc::op_desc_sw128(smb + ((ks >> 2) ? KP3 : KP2), k0);
-                tc::mma_f16_ta(tm + TM_U, ash, wh, id64n, true);
-                tc::mma_f16_ta(tm + TM_U, ash, wl, id64n, true);
-                tc::mma_f16_ta(tm + TM_U, asl, wh, id64n, true);
-                const uint32_t at = (ks >> 2) * 16384 + 8192;  // rows 64-127 (Q) of the atom
-                const uint64_t qh = tc::op_desc_sw128(smb + S_KQH + at, k0);
-                const uint64_t ql = tc::op_desc_sw128(smb + S_KQL + at, k0);
-                tc::mma_f16_ta(tm + TM_G, ash, qh, id64, ks > 0);
-                tc::mma_f16_ta(tm + TM_G, ash, ql, id64, true);
-                tc::mma_f16_ta(tm + TM_G, asl, qh, id64, true);
-            }
+            mma3t(tm + TM_X3, tm + TM_SH, tm + TM_SL, smb + S_KQH, smb + S_KQL, QLBO, QSBO, D, id128, false);
             tc::mma_commit(&ps.mma_bar);
         }
-        mma_wait();
+        mma_wait(true);
 
-        // ---- V_new and V_new diag(e^{G_last - G} rk) operands [j][s]; S^T <- e^{G_last} S^T
+        // ---- V_new = U - PW and V_new diag(e^{G_last - G} rk), fp16 hi / lo, into TMEM
         {
-            const int j = lb + lane;
-            float v[16], vd[16];
-            tc::tmem_ld16(tc::taddr(tm, lb, TM_U + 16 * part), v);
+            float u[16], pw[16];
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_U + 16 * part), u);
+            tc::tmem_ld16(tc::taddr(tm, lb, TM_X3 + 16 * part), pw);
+            uint32_t nh[8], nl[8], dh[8], dl[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) vd[k] = v[k] * ps.ds[16 * part + k];
-            put8(sm + S_VNH, sm + S_VNL, cano(j, 16 * part, 1024), v);
-            put8(sm + S_VNH, sm + S_VNL, cano(j, 16 * part + 8, 1024), v + 8);
-            put8(sm + S_VDH, sm + S_VDL, cano(j, 16 * part, 1024), vd);
-            put8(sm + S_VDH, sm + S_VDL, cano(j, 16 * part + 8, 1024), vd + 8);
-            const float gl = ps.egl;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float s[16];
-                tc::tmem_ld16(tc::taddr(tm, lb, TM_S + 32 * part + 16 * q), s);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) s[k] *= gl;
-                tc::tmem_st16(tc::taddr(tm, lb, TM_S + 32 * part + 16 * q), s);
+            for (int k = 0; k < 8; ++k) {
+                const float v0 = u[2 * k] - pw[2 * k], v1 = u[2 * k + 1] - pw[2 * k + 1];
+                split2(v0, v1, nh[k], nl[k]);
+                split2(v0 * ps.ds[16 * part + 2 * k], v1 * ps.ds[16 * part + 2 * k + 1], dh[k], dl[k]);
             }
+            tmem_st8u_nowait(tc::taddr(tm, lb, TM_VNH + 8 * part), nh);
+            tmem_st8u_nowait(tc::taddr(tm, lb, TM_VNL + 8 * part), nl);
+            tmem_st8u_nowait(tc::taddr(tm, lb, TM_VDH + 8 * part), dh);
+            tmem_st8u_nowait(tc::taddr(tm, lb, TM_VDL + 8 * part), dl);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        publish();  // B5
+        tc::fence_before_sync();
+        __syncthreads();  // B5
 
-        // ---- OV^T = V_new^T M^T;  S^T += (V_new diag(d))^T K
+        // ---- OV = V_new^T M^T;  S^T += (V_new diag(d))^T K
         if (tid == 0) {
             tc::fence_after_sync();
-            mma3c(tm + TM_OV, smb + S_VNH, smb + S_VNL, 1024, smb + S_MH, smb + S_ML, 1024, CK, id64, false);
-            mma3c(tm + TM_S, smb + S_VDH, smb + S_VDL, 1024, smb + S_KTH, smb + S_KTL, TSBO, CK, id128, true);
+            mma3t(tm + TM_X1, tm + TM_VNH, tm + TM_VNL, smb + S_MH, smb + S_ML, 128, 1024, CK, id64, false);
+            mma3t(tm + TM_S, tm + TM_VDH, tm + TM_VDL, smb + S_KTH, smb + S_KTL, 128, TSBO, CK, id128, true);
             tc::mma_commit(&ps.mma_bar);
         }
-        mma_wait();
+        mma_wait(true);
         cp = c0;
         np = n;
     }
 
     // the last chunk's output, the final state and the conv window
     const int nchunks = (T + CK - 1) / CK;
-    if (warp >= 12) epilogue(cp, np, nchunks - 1);
+    if (!grp_a) epilogue(cp, np, nchunks - 1);
     {
         float *So = a.state_out + head * D * D;
 #pragma unroll

@@ -158,6 +158,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Waits for phase `parity` of `bar` with mbarrier.try_wait, which suspends the
+// thread in hardware until the phase completes or a short time limit passes, so a
+// waiting warp takes no issue slots from the working ones.  Gives up after about
+// 2^32 clock cycles (two seconds at 2 GHz) and returns false (the caller records
+// an error and goes on).
+__device__ __forceinline__ bool mbar_wait_suspend_bounded(uint64_t *bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > (1LL << 32)) return false;
+    }
+}
+
 // Waits (acquire at cluster scope) for phase `parity` of a local mbarrier that
 // remote CTAs complete with st.async; gives up after about two seconds.
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity)
