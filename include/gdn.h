@@ -129,8 +129,10 @@ typedef struct {
     float *conv_state;     /* [B,conv_K-1,C], oldest row first                    */
     float *state;          /* [B,H_v,d_k,d_v]; row = key channel                  */
     void *out;             /* [B,T,H_v*d_v] out_dtype                             */
-    float *state_hist;     /* verify: [T,B,H_v,d_k,d_v] or NULL; otherwise unused */
-    float *conv_hist;      /* verify: [T,B,conv_K-1,C] or NULL; otherwise unused  */
+    float *state_hist;     /* verify: [T,B,H_v,d_k,d_v]; prefill: [min(T,4),B,H_v,d_k,d_v]
+                              (snapshot tails); or NULL; unused elsewhere        */
+    float *conv_hist;      /* verify: [T,B,conv_K-1,C]; prefill: [min(T,4),B,conv_K-1,C];
+                              or NULL; unused elsewhere                          */
 } gdn_tensors_t;
 
 /*
@@ -175,13 +177,26 @@ GDN_API gdn_status_t gdn_commit_accepted(const gdn_shape_t *shape, const gdn_ten
  * Chunked prefill of T >= 1 tokens per sequence: the same result as T decode
  * steps, computed in the chunked WY/UT form ("llama.cpp PR #84", chunked
  * KDA prefill).  conv_state and state are advanced in place; out receives y
- * for every token.  At d = 128 and T > 4 the two-kernel form runs (an
- * intra-chunk pass over all 16-token chunks, then a tcgen05 state pass),
- * whatever shape->chunk asks (which must be > 0), except that shape->chunk == 32
- * with the per-head decay and bf16 rows runs the single tensor-core kernel in
- * 32-token chunks; other shapes run the recurrent kernel.  workspace must hold gdn_prefill_workspace_bytes(shape)
- * bytes, 16-byte aligned (may be 0 bytes; then NULL is accepted); the call
- * owns it until the work queued on `stream` completes.
+ * for every token.  Kernels, by shape (shape->chunk must be > 0):
+ *   - per-head decay, bf16 rows, d = 128, chunk == 64: one tensor-core kernel
+ *     in 64-token chunks, every dense product on tcgen05, no workspace;
+ *   - the same with chunk == 32: one tensor-core kernel in 32-token chunks;
+ *   - any other shape with d = 128 and T > 4 (per-channel decay, fp32 rows,
+ *     other chunk lengths): the two-kernel form, an intra-chunk pass over all
+ *     16-token chunks into the workspace, then a tcgen05 state pass;
+ *   - everything else: the recurrent step kernel.
+ * workspace must hold gdn_prefill_workspace_bytes(shape) bytes, 16-byte aligned
+ * (may be 0 bytes; then NULL is accepted); the call owns it until the work
+ * queued on `stream` completes.
+ *
+ * Snapshot tails ("llama.cpp PR #84", the chunked prefill's snapshot slots):
+ * when state_hist or conv_hist is not NULL, the first T - n tokens (n =
+ * min(T, 4)) run as above and the last n on the recurrent step kernel from the
+ * state and window they leave; state_hist[k] ([n,B,H_v,d_k,d_v], 16-byte
+ * aligned) then receives the state after token T - n + k and conv_hist[k]
+ * ([n,B,conv_K-1,C]) the conv window after it, so index n - 1 holds the final
+ * state and window (also left in state and conv_state).  A caller rolls back
+ * to any of the last n tokens by adopting those entries.
  */
 GDN_API gdn_status_t gdn_prefill_chunked(const gdn_shape_t *shape, const gdn_tensors_t *t,
                                  void *workspace, size_t workspace_bytes,

@@ -91,6 +91,7 @@ gdn::StepArgs step_args(const gdn_shape_t *s, const gdn_tensors_t *t)
     a.out = t->out;
     a.B = s->B;
     a.T = s->T;
+    a.Ts = s->T;
     a.H_qk = s->H_qk;
     a.H_v = s->H_v;
     a.C = 2 * s->H_qk * s->d_k + s->H_v * s->d_v;
@@ -155,6 +156,22 @@ void *static_scratch()
     c.ptr = p;
     c.ctx = ctx;
     return p;
+}
+
+// The prefill after its checks: with snapshot tails when state_hist or conv_hist is set.
+gdn_status_t prefill_call(const gdn_shape_t *s, const gdn_tensors_t *t, void *workspace,
+                          cudaStream_t stream)
+{
+    gdn::StepArgs a = step_args(s, t);
+    a.state_out = t->state;
+    a.conv_out = t->conv_state;
+    const int sms = num_sms_current();
+    if (t->state_hist || t->conv_hist) {
+        a.state_hist = t->state_hist;
+        a.conv_hist = t->conv_hist;
+        return gdn::run_prefill_snapshots(*s, a, workspace, sms > 0 ? sms : 148, stream);
+    }
+    return gdn::run_prefill(*s, a, workspace, sms > 0 ? sms : 148, stream);
 }
 
 gdn_status_t run_step(const gdn_shape_t *s, const gdn::StepArgs &a, cudaStream_t stream)
@@ -239,16 +256,13 @@ gdn_status_t gdn_prefill_chunked(const gdn_shape_t *s, const gdn_tensors_t *t, v
     rc = check_tensors(s, t);
     if (rc != GDN_OK) return rc;
     if (s->chunk <= 0) return GDN_ERR_SHAPE;
+    if ((t->state_hist && !aligned16(t->state_hist)) || (t->conv_hist && !aligned(t->conv_hist, 4)))
+        return GDN_ERR_ALIGN;
     const size_t need = gdn::prefill_workspace_bytes(*s);
     if (workspace_bytes < need || (need > 0 && !workspace)) return GDN_ERR_WORKSPACE;
     if (workspace && !aligned16(workspace)) return GDN_ERR_ALIGN;
     if (s->B == 0) return GDN_OK;
-    gdn::StepArgs a = step_args(s, t);
-    a.state_out = t->state;
-    a.conv_out = t->conv_state;
-    const int sms = num_sms_current();
-    return gdn::run_prefill(*s, a, workspace, sms > 0 ? sms : 148,
-                            reinterpret_cast<cudaStream_t>(stream));
+    return prefill_call(s, t, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *s, const gdn_tensors_t *t,
@@ -260,6 +274,8 @@ gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *s, const gdn_tensors_
     rc = check_tensors(s, t);
     if (rc != GDN_OK) return rc;
     if (s->chunk <= 0) return GDN_ERR_SHAPE;
+    if ((t->state_hist && !aligned16(t->state_hist)) || (t->conv_hist && !aligned(t->conv_hist, 4)))
+        return GDN_ERR_ALIGN;
     const size_t need = gdn::prefill_workspace_bytes(*s);
     if (need > GDN_PREFILL_STATIC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
     if (s->B == 0) return GDN_OK;
@@ -269,11 +285,7 @@ gdn_status_t gdn_prefill_chunked_static(const gdn_shape_t *s, const gdn_tensors_
         if (!ws) return GDN_ERR_CUDA;
     }
     // no clearing: the intra-chunk kernel writes every scratch word the state kernel uses
-    gdn::StepArgs a = step_args(s, t);
-    a.state_out = t->state;
-    a.conv_out = t->conv_state;
-    const int sms = num_sms_current();
-    return gdn::run_prefill(*s, a, ws, sms > 0 ? sms : 148, reinterpret_cast<cudaStream_t>(stream));
+    return prefill_call(s, t, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t gdn_layer_workspace_bytes(const gdn_shape_t *s, const gdn_layer_weights_t *w)

@@ -257,7 +257,7 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
     const int quad = warp & 3, part = warp >> 2, lb = 32 * quad;
     const bool grp_a = warp < 8;  // warps 0-7: Gram, A, inverse; 8-15: state copy, output
     const int h = blockIdx.x, b = blockIdx.y, hq = h / a.group;
-    const int T = a.T, C = a.C, H = a.H_v;
+    const int T = a.T, Ts = a.Ts, C = a.C, H = a.H_v;
     const bool clustered = a.group > 1;
     const bool qk_owner = (h % a.group) == 0;
     const size_t head = static_cast<size_t>(b) * H + h;
@@ -287,7 +287,7 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
     // this chunk's q, k, v rows and the 3 before them: three [67][128] boxes of [B*T, C]
     auto issue_raw = [&](int c0) {
         mbar_expect_tx(&ps.raw_full, 3 * RAW_BOX);
-        const int row = b * T + c0 - 3;  // rows before the tensor read as zero
+        const int row = b * Ts + c0 - 3;  // rows before the tensor read as zero
         tma_load_2d(sm + S_RAW, &tm_qkv, chq, row, &ps.raw_full);
         tma_load_2d(sm + S_RAW + RAW_BOX, &tm_qkv, chk, row, &ps.raw_full);
         tma_load_2d(sm + S_RAW + 2 * RAW_BOX, &tm_qkv, chv, row, &ps.raw_full);
@@ -334,7 +334,7 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
         for (int u = 0; u < 2; ++u) {
             const int t = c0 + 2 * lane + u;
             if (t < T) {
-                const size_t e = (static_cast<size_t>(b) * T + t) * H + h;
+                const size_t e = (static_cast<size_t>(b) * Ts + t) * H + h;
                 fx[u] = ld_in(a.f, e, 1);
                 bx[u] = ld_in(a.beta, e, 1);
             }
@@ -381,20 +381,33 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
             ps.rinv[t] = rsqrtf(m + a.eps_norm);
         }
         bar_b();
-        const unsigned char *zs = sm + S_Z;
+        // y = o rinv w gate(z) for the 32 tokens, then the stores (row stride H * D)
+        const unsigned char *zs = sm + S_Z + (32 * th * D + j) * 2;
+        const bool sig = a.sig_gate != 0;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const int t = 32 * th + k;
-            if (t < np) {
-                const float zz = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(zs + (t * D + j) * 2));
-                const float gz = a.sig_gate ? sigmoid_fast(zz) : silu_fast(zz);
-                const float y = o[k] * ps.rinv[t] * nw * gz;
-                const size_t idx = ((static_cast<size_t>(b) * T + cp + t) * H + h) * D + j;
-                if (a.out_bf16)
-                    reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(y);
-                else
-                    reinterpret_cast<float *>(a.out)[idx] = y;
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+            const float4 r4 = *reinterpret_cast<const float4 *>(&ps.rinv[32 * th + k4]);
+            const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float zz = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(zs + (k4 + k) * D * 2));
+                const float e = __expf(-zz);
+                const float gz = __fdividef(sig ? 1.0f : zz, 1.0f + e);
+                o[k4 + k] *= rv[k] * nw * gz;
             }
+        }
+        const size_t row0 = (static_cast<size_t>(b) * Ts + cp + 32 * th) * H + h;
+        const int nk = min(32, np - 32 * th);  // tokens of this half inside the chunk
+        if (a.out_bf16) {
+            __nv_bfloat16 *yo = reinterpret_cast<__nv_bfloat16 *>(a.out) + row0 * D + j;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (k < nk) yo[static_cast<size_t>(k) * H * D] = __float2bfloat16_rn(o[k]);
+        } else {
+            float *yo = reinterpret_cast<float *>(a.out) + row0 * D + j;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (k < nk) yo[static_cast<size_t>(k) * H * D] = o[k];
         }
         fence_proxy_async_smem();  // the z stage is read: the next copy may land there
     };
@@ -633,7 +646,7 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
         publish();  // B2
         if (tid == 0) {  // the previous output has read the z stage: this chunk's rows
             mbar_expect_tx(&ps.z_full, CK * D * 2);
-            tma_load_3d(sm + S_Z, &tm_z, 0, h, b * T + c0, &ps.z_full);
+            tma_load_3d(sm + S_Z, &tm_z, 0, h, b * Ts + c0, &ps.z_full);
         }
 
         // ---- T1 = T diag(beta e^G rk), T2 = T diag(beta): [64 t][64 s] into the K rows
@@ -759,7 +772,7 @@ c64_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qkv,
 #pragma unroll
             for (int r = 0; r < 3; ++r) {
                 const int tau = T - 3 + r;
-                v[r] = tau >= 0 ? ld_in(a.qkv, (static_cast<size_t>(b) * T + tau) * C + ch, 1)
+                v[r] = tau >= 0 ? ld_in(a.qkv, (static_cast<size_t>(b) * Ts + tau) * C + ch, 1)
                                 : win[(3 + tau) * NCONV + tid];
             }
 #pragma unroll
@@ -802,7 +815,7 @@ cudaError_t launch_c64(const StepArgs &a, cudaStream_t stream)
         attr_set[dev] = true;
     }
     CUtensorMap tq, tz;
-    const uint64_t rows = static_cast<uint64_t>(a.B) * a.T;
+    const uint64_t rows = static_cast<uint64_t>(a.B) * a.Ts;
     {   // qkv as [B*T rows][C channels] bf16, boxes of 67 rows x 128 channels
         const uint64_t dim[2] = {static_cast<uint64_t>(a.C), rows};
         const uint64_t stride[1] = {static_cast<uint64_t>(a.C) * 2};

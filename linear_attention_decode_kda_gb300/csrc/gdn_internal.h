@@ -20,6 +20,7 @@ struct StepArgs {
     float *conv_hist;            // [T,B,K-1,C] or NULL
     const int32_t *accepted;     // [B]: tokens taken per sequence (clamped to 0..T), or NULL for T
     int B, T, H_qk, H_v, C;
+    int Ts;                      // token stride of the [B, Ts, ...] rows: T, or more for a part of a call
     int group;                   // H_v / H_qk
     int kda;                     // one decay per key channel (both per-channel gate forms)
     int lb_gate;                 // lower-bound gate: A_log = scale a, dt_bias[h] = bound lb

@@ -144,7 +144,7 @@ kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensor
     const int nt = min(KC, a.T - t0);
     const int hq = h / a.group;
     const size_t C = static_cast<size_t>(a.C);
-    const size_t row0 = static_cast<size_t>(b) * a.T + t0;
+    const size_t row0 = static_cast<size_t>(b) * a.Ts + t0;
     auto ld = [&](const void *p, size_t idx) {
         return BF16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[idx])
                     : reinterpret_cast<const float *>(p)[idx];
@@ -157,10 +157,10 @@ kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensor
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             const int tau = t0 - 3 + j;
-            x[j] = tau >= 0 ? ld(a.qkv, (static_cast<size_t>(b) * a.T + tau) * C + c)
+            x[j] = tau >= 0 ? ld(a.qkv, (static_cast<size_t>(b) * a.Ts + tau) * C + c)
                             : a.conv_in[(static_cast<size_t>(b) * 3 + (3 + tau)) * C + c];
         }
-        const size_t base = static_cast<size_t>(b) * a.T;
+        const size_t base = static_cast<size_t>(b) * a.Ts;
 #pragma unroll
         for (int t = 0; t < KC; ++t) x[3 + t] = ld(a.qkv, (base + min(t0 + t, a.T - 1)) * C + c);
     };
@@ -188,12 +188,12 @@ kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensor
         __syncthreads();
         if (tid == 0) {
             unsigned char *dst = reinterpret_cast<unsigned char *>(&stg[0][0][0]);
-            const int row = b * a.T + t0 - 3;  // rows before the batch read as zero
+            const int row = b * a.Ts + t0 - 3;  // rows before the batch read as zero
             mbar_expect_tx(&raw_bar, 3 * RAW_SEG + (PER_CHANNEL ? KC * KD * 2 : 0));
             tma_load_2d(dst, &tq, chq, row, &raw_bar);
             tma_load_2d(dst + RAW_SEG, &tq, chk, row, &raw_bar);
             tma_load_2d(dst + 2 * RAW_SEG, &tq, chv, row, &raw_bar);
-            if (PER_CHANNEL) tma_load_3d(dst + 3 * RAW_SEG, &tf, 0, h, b * a.T + t0, &raw_bar);
+            if (PER_CHANNEL) tma_load_3d(dst + 3 * RAW_SEG, &tf, 0, h, b * a.Ts + t0, &raw_bar);
         }
     }
     // channel i of box sg: rows t0 - 3 .. t0 + 15, the first three from the kept
@@ -215,7 +215,7 @@ kda_intra_kernel(StepArgs a, unsigned char *ws, const __grid_constant__ CUtensor
     if (tid >= KD && !(BF16 && PER_CHANNEL)) {
 #pragma unroll
         for (int t = 0; t < KC; ++t) {
-            const size_t bth = (static_cast<size_t>(b) * a.T + min(t0 + t, a.T - 1)) * a.H_v + h;
+            const size_t bth = (static_cast<size_t>(b) * a.Ts + min(t0 + t, a.T - 1)) * a.H_v + h;
             fl[t] = PER_CHANNEL ? ld(a.f, bth * KD + i) : ld(a.f, bth);
         }
     }
@@ -515,7 +515,7 @@ kda_state_kernel(StepArgs a, const unsigned char *ws, int nchunk, const __grid_c
             mbar_expect_tx(&ps.full[s], BLOCK_BYTES + zbytes);
             tma_load_1d(sm + s * STAGE, blocks + static_cast<size_t>(n) * BLOCK_BYTES, BLOCK_BYTES, &ps.full[s]);
             // rows past the last token of the batch read as zero; rows of the next sequence are unused
-            tma_load_3d(sm + s * STAGE + STAGE_Z, &tmz, 0, h, b * a.T + n * KC, &ps.full[s]);
+            tma_load_3d(sm + s * STAGE + STAGE_Z, &tmz, 0, h, b * a.Ts + n * KC, &ps.full[s]);
         };
         // descriptors: S^T (A, K = 128) and stage 0's [W; e^G Q] (B, K = 128); the
         // K = 16 operands V_new^T (A), A (B) and (e^{G_last-G} K)^T (B)
@@ -666,7 +666,7 @@ kda_state_kernel(StepArgs a, const unsigned char *ws, int nchunk, const __grid_c
             for (int j = 0; j < 8; ++j) {
                 const int t = 8 * half + j;
                 if (t < nt) {
-                    const size_t idx = ((static_cast<size_t>(b) * a.T + t0 + t) * a.H_v + h) * KD + ch;
+                    const size_t idx = ((static_cast<size_t>(b) * a.Ts + t0 + t) * a.H_v + h) * KD + ch;
                     const float yv = o[j] * ps.rinv[t] * gz[j];
                     if (a.out_bf16)
                         reinterpret_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(yv);
@@ -705,7 +705,7 @@ kda_state_kernel(StepArgs a, const unsigned char *ws, int nchunk, const __grid_c
                 for (int j = 0; j < 3; ++j) {
                     const int idx = a.T + j;
                     x3[j] = idx < 3 ? a.conv_in[(static_cast<size_t>(b) * 3 + idx) * C + c]
-                                    : ld_in(a.qkv, (static_cast<size_t>(b) * a.T + idx - 3) * C + c, a.in_bf16);
+                                    : ld_in(a.qkv, (static_cast<size_t>(b) * a.Ts + idx - 3) * C + c, a.in_bf16);
                 }
 #pragma unroll
                 for (int j = 0; j < 3; ++j) a.conv_out[(static_cast<size_t>(b) * 3 + j) * C + c] = x3[j];
@@ -779,7 +779,7 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
     CUtensorMap tmz;
     {   // z as [B*T][H_v][128] in the input dtype, boxes of 16 tokens x 1 head x 128 channels
         const uint64_t es = a.in_bf16 ? 2 : 4;
-        const uint64_t dim[3] = {KD, static_cast<uint64_t>(a.H_v), static_cast<uint64_t>(a.B) * a.T};
+        const uint64_t dim[3] = {KD, static_cast<uint64_t>(a.H_v), static_cast<uint64_t>(a.B) * a.Ts};
         const uint64_t stride[2] = {KD * es, static_cast<uint64_t>(a.H_v) * KD * es};
         const uint32_t box[3] = {KD, 1, KC};
         if (!encode_tiled(&tmz, a.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
@@ -789,14 +789,14 @@ cudaError_t launch_kda_chunked(const StepArgs &a, void *workspace, cudaStream_t 
     CUtensorMap tq = {}, tf = {};
     if (a.in_bf16) {
         {   // qkv as [B*T rows][C channels], boxes of 19 rows x 128 channels
-            const uint64_t dim[2] = {static_cast<uint64_t>(a.C), static_cast<uint64_t>(a.B) * a.T};
+            const uint64_t dim[2] = {static_cast<uint64_t>(a.C), static_cast<uint64_t>(a.B) * a.Ts};
             const uint64_t stride[1] = {static_cast<uint64_t>(a.C) * 2};
             const uint32_t box[2] = {KD, RAW_ROWS};
             if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qkv, dim, stride, box))
                 return cudaErrorInvalidValue;
         }
         if (a.kda) {  // per-channel gate rows as [B*T][H_v][128], boxes of 16 tokens
-            const uint64_t dim[3] = {KD, static_cast<uint64_t>(a.H_v), static_cast<uint64_t>(a.B) * a.T};
+            const uint64_t dim[3] = {KD, static_cast<uint64_t>(a.H_v), static_cast<uint64_t>(a.B) * a.Ts};
             const uint64_t stride[2] = {KD * 2, static_cast<uint64_t>(a.H_v) * KD * 2};
             const uint32_t box[3] = {KD, 1, KC};
             if (!encode_tiled(&tf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.f, dim, stride, box))

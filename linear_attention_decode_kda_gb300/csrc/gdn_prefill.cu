@@ -126,7 +126,7 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
     const int ch = tid & (PD - 1);  // channel / TMEM lane of this thread
     const int lb = 32 * quad;       // this warp's TMEM lane quadrant
     const int h = blockIdx.x, b = blockIdx.y, hq = h / a.group;
-    const int T = a.T, C = a.C, H = a.H_v;
+    const int T = a.T, Ts = a.Ts, C = a.C, H = a.H_v;
     const bool clustered = a.group > 1;
     const bool qk_owner = (h % a.group) == 0;
     const size_t head = static_cast<size_t>(b) * H + h;
@@ -191,7 +191,7 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
         if (lane == 0) {
             fence_proxy_async_smem();
             mbar_expect_tx(&ps.raw_full, 3 * CH * PD * 2);
-            const int row = b * T + c0;
+            const int row = b * Ts + c0;
             tma_load_2d(raw, &tm_qkv, chq, row, &ps.raw_full);
             tma_load_2d(raw + CH * PD * 2, &tm_qkv, chk, row, &ps.raw_full);
             tma_load_2d(raw + 2 * CH * PD * 2, &tm_qkv, chv, row, &ps.raw_full);
@@ -202,7 +202,7 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
         if (lane == 0) {
             fence_proxy_async_smem();
             mbar_expect_tx(&ps.z_full, CH * PD * 2);
-            tma_load_3d(zs, &tm_z, 0, h, b * T + c0, &ps.z_full);
+            tma_load_3d(zs, &tm_z, 0, h, b * Ts + c0, &ps.z_full);
         }
     };
     if (warp == 0) {
@@ -212,7 +212,7 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
     // gate logits of the next chunk, one token per lane of warp 0
     float f_nx = 0.f, b_nx = 0.f;
     if (tid < CH && tid < T) {
-        const size_t e = (static_cast<size_t>(b) * T + tid) * H + h;
+        const size_t e = (static_cast<size_t>(b) * Ts + tid) * H + h;
         f_nx = ld_in(a.f, e, 1);
         b_nx = ld_in(a.beta, e, 1);
     }
@@ -238,7 +238,7 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
                 bt = sigmoid_f(b_nx);
             }
             if (c0 + CH + lane < T) {  // next chunk's logits, in flight during this one
-                const size_t e = (static_cast<size_t>(b) * T + c0 + CH + lane) * H + h;
+                const size_t e = (static_cast<size_t>(b) * Ts + c0 + CH + lane) * H + h;
                 f_nx = ld_in(a.f, e, 1);
                 b_nx = ld_in(a.beta, e, 1);
             }
@@ -502,7 +502,7 @@ chunk_prefill_kernel(const StepArgs a, const __grid_constant__ CUtensorMap tm_qk
             const int e = tid + PT * k4, t = e / (PD / 4), c4 = 4 * (e % (PD / 4));
             if (t < n) {
                 const float4 y4 = *reinterpret_cast<const float4 *>(ys + t * YS + c4);
-                const size_t idx = ((static_cast<size_t>(b) * T + c0 + t) * H + h) * PD + c4;
+                const size_t idx = ((static_cast<size_t>(b) * Ts + c0 + t) * H + h) * PD + c4;
                 store_out4(a.out, idx, a.out_bf16, y4.x, y4.y, y4.z, y4.w);
             }
         }
@@ -586,7 +586,7 @@ cudaError_t launch_chunked(const StepArgs &a, cudaStream_t stream)
         attr_set[dev] = true;
     }
     CUtensorMap tq, tz;
-    const uint64_t rows = static_cast<uint64_t>(a.B) * a.T;
+    const uint64_t rows = static_cast<uint64_t>(a.B) * a.Ts;
     {   // qkv as [B*T rows][C channels] bf16, boxes of CH rows x PD channels
         const uint64_t dim[2] = {static_cast<uint64_t>(a.C), rows};
         const uint64_t stride[1] = {static_cast<uint64_t>(a.C) * 2};
@@ -661,6 +661,42 @@ gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspac
                                   : plan_slab_one_wave(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan);
     if (!planned) return GDN_ERR_UNSUPPORTED;
     cudaError_t e = launch_step(plan, a, (s.flags & GDN_FLAG_PDL) != 0, num_sms, stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t run_prefill_snapshots(const gdn_shape_t &s, const StepArgs &a, void *workspace,
+                                   int num_sms, cudaStream_t stream)
+{
+    const int n = s.T < 4 ? s.T : 4, Tm = s.T - n;
+    if (Tm > 0) {  // the head of each sequence: rows 0 .. Tm - 1 of the [B, T, ...] tensors
+        gdn_shape_t sm = s;
+        sm.T = Tm;
+        StepArgs am = a;
+        am.T = Tm;
+        am.state_hist = nullptr;
+        am.conv_hist = nullptr;
+        const gdn_status_t rc = run_prefill(sm, am, workspace, num_sms, stream);
+        if (rc != GDN_OK) return rc;
+    }
+    // the tail: rows Tm .. T - 1, from the state and window the head left in place
+    const size_t es = a.in_bf16 ? 2 : 4, os = a.out_bf16 ? 2 : 4, d = s.d_k;
+    const size_t fw = a.kda ? d : 1;
+    StepArgs at = a;
+    at.T = n;
+    at.Ts = s.T;
+    at.qkv = static_cast<const char *>(a.qkv) + static_cast<size_t>(Tm) * a.C * es;
+    at.f = static_cast<const char *>(a.f) + static_cast<size_t>(Tm) * a.H_v * fw * es;
+    at.beta = static_cast<const char *>(a.beta) + static_cast<size_t>(Tm) * a.H_v * es;
+    at.z = static_cast<const char *>(a.z) + static_cast<size_t>(Tm) * a.H_v * d * es;
+    at.out = static_cast<char *>(a.out) + static_cast<size_t>(Tm) * a.H_v * d * os;
+    at.state_in = a.state_out;
+    at.conv_in = a.conv_out;
+    at.accepted = nullptr;
+    StepPlan plan;
+    if (!plan_slab(s.d_k, s.B, s.H_v, s.H_v / s.H_qk, num_sms, &plan)) return GDN_ERR_UNSUPPORTED;
+    // plain stream order: the head (when there is one) writes the state the tail reads first
+    const bool pdl = Tm == 0 && (s.flags & GDN_FLAG_PDL) != 0;
+    const cudaError_t e = launch_slab(plan, at, pdl, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -19,6 +19,13 @@ const char *prefill_variant(const gdn_shape_t &s, int num_sms);
 gdn_status_t run_prefill(const gdn_shape_t &s, const StepArgs &a, void *workspace, int num_sms,
                          cudaStream_t stream);
 
+// The prefill with snapshot tails: the first T - n tokens (n = min(T, 4)) as
+// run_prefill, then the last n on the recurrent step kernel, which writes
+// a.state_hist / a.conv_hist after each of them and leaves the final state and
+// window in place.  `a` carries the tensors with state_out / conv_out set.
+gdn_status_t run_prefill_snapshots(const gdn_shape_t &s, const StepArgs &a, void *workspace,
+                                   int num_sms, cudaStream_t stream);
+
 // Reads and clears the chunked prefill kernel's device error word (synchronous).
 unsigned int take_prefill_error();
 

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         const size_t esz = a.in_bf16 ? 2 : 4;
         const char *qkv = static_cast<const char *>(a.qkv);
         for (int s = warp; s < 6 * ntok; s += NWARP) {
-            const size_t bt = static_cast<size_t>(b) * a.T + s / 6;
+            const size_t bt = static_cast<size_t>(b) * a.Ts + s / 6;
             const size_t row = bt * C, bth = bt * a.H_v + h;
             const void *p = nullptr;
             size_t n = 0;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
 
     // All inputs of token t in one round of independent loads.
     auto load_token = [&](int t, TokenIn<CQ, CV> &in) {
-        const size_t bt = static_cast<size_t>(b) * a.T + t;
+        const size_t bt = static_cast<size_t>(b) * a.Ts + t;
         const size_t row = bt * C;
         const size_t bth = bt * a.H_v + h;
 #pragma unroll
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         if (t > 0) __syncthreads();  // previous token's shared-memory reads are done
         TokenIn<CQ, CV> nxt;
         if (t + 1 < Tb) load_token(t + 1, nxt);
-        const size_t bth = (static_cast<size_t>(b) * a.T + t) * a.H_v + h;
+        const size_t bth = (static_cast<size_t>(b) * a.Ts + t) * a.H_v + h;
 
         // 1. conv + SiLU, norms' partial sums, gates
         float sq = 0.f, sk = 0.f, sqk = 0.f;
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
         const size_t esz = a.in_bf16 ? 2 : 4;
         const char *qkv = static_cast<const char *>(a.qkv);
         for (int s = warp; s < 6 * ntok; s += NW) {
-            const size_t bt = static_cast<size_t>(b) * a.T + s / 6;
+            const size_t bt = static_cast<size_t>(b) * a.Ts + s / 6;
             const size_t row = bt * C, bth = bt * a.H_v + h;
             const void *p = nullptr;
             size_t n = 0;
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
     pdl_launch_dependents();
 
     auto load_token = [&](int t, WIn &in) {
-        const size_t bt = static_cast<size_t>(b) * a.T + t;
+        const size_t bt = static_cast<size_t>(b) * a.Ts + t;
         const size_t row = bt * C, bth = bt * a.H_v + h;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
     for (int t = 0; t < Tb; ++t) {
         WIn nxt;
         if (t + 1 < Tb) load_token(t + 1, nxt);
-        const size_t bth = (static_cast<size_t>(b) * a.T + t) * a.H_v + h;
+        const size_t bth = (static_cast<size_t>(b) * a.Ts + t) * a.H_v + h;
 
         // 1. conv + SiLU of the lane's q/k channels, their decay, v of column jc, beta
         float q[4], k[4], al[4];

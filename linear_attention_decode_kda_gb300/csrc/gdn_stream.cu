@@ -455,7 +455,7 @@ bool stream_eligible(const StepArgs &a)
     bool ok = aligned16(a.qkv) && (static_cast<size_t>(a.C) * es) % 16 == 0 && aligned16(a.z) &&
               aligned16(a.conv_in) && aligned16(a.conv_w) && aligned16(a.beta) && aligned16(a.f) &&
               aligned16(a.dt_bias) && aligned16(a.A_log) && rows16 && a.H_qk == a.H_v;
-    return ok && a.T >= 1 && a.T <= MAX_T && static_cast<long long>(a.B) * a.T * KM1 < (1LL << 31);
+    return ok && a.T >= 1 && a.T <= MAX_T && a.Ts == a.T && static_cast<long long>(a.B) * a.T * KM1 < (1LL << 31);
 }
 
 bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)

@@ -131,6 +131,20 @@ def test_prefill_workspace_checks(lib):
     assert gdn.gdn_prefill_workspace_bytes(bad) == 0
 
 
+def test_prefill_snapshot_buffers_are_checked(lib):
+    """Snapshot tails: state_hist must be 16-byte aligned and conv_hist 4-byte
+    aligned, in gdn_prefill_chunked and gdn_prefill_chunked_static alike, before
+    anything is queued."""
+    s = _shape(T=100, kda=True)
+    need = gdn.gdn_prefill_workspace_bytes(s)
+    for field, off in (("state_hist", 4), ("conv_hist", 2)):
+        t = _tensors()
+        setattr(t, field, getattr(t, field) + off)
+        assert _call(lib, "prefill", s, t, 0x100000, need) == gdn.GDN_ERR_ALIGN
+        s1 = _shape(T=30, kda=True)
+        assert lib.gdn_prefill_chunked_static(ctypes.byref(s1), ctypes.byref(t), None) == gdn.GDN_ERR_ALIGN
+
+
 def test_status_strings(lib):
     for code in range(-7, 1):
         assert gdn.status_string(code).startswith("GDN_")
