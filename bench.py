@@ -486,6 +486,9 @@ class LayerDecode(Workload):
 
 LAYER_WORKLOADS = {"kda_layer_decode_b1": 1, "kda_layer_decode_b64": 64}
 
+# The 34-layer decode chain at a middle batch (8 sequences), 16 distinct tokens cycled.
+MIDBATCH_WORKLOADS = {"kda_decode_b8_34layers": 8}
+
 # The verify workload's two calls of a speculative step without per-token states:
 # a verify that writes outputs only, then the in-place commit of the accepted tokens.
 EXTRA_WORKLOADS = {"kda_verify_b32_t4_outputs_only": ("kda_verify_b32_t4", "verify_outputs"),
@@ -507,6 +510,10 @@ def make_workload(name, device):
     spec = synth.WORKLOADS.get(name)
     if name == "kda_decode_b1_34layers":
         return DecodeLayers(name, spec, device)
+    if name in MIDBATCH_WORKLOADS:
+        spec = dict(synth.WORKLOADS["kda_decode_b1_34layers"])
+        spec["shape"] = dataclasses.replace(spec["shape"], B=MIDBATCH_WORKLOADS[name])
+        return DecodeLayers(name, spec, device, tokens=16)
     if name in EXTRA_WORKLOADS:
         base, mode = EXTRA_WORKLOADS[name]
         spec = dict(synth.WORKLOADS[base])
@@ -770,13 +777,15 @@ def run_ours(args):
 
     if rank == 0 and not args.no_workloads:
         extra = {}
-        for name in ("kda_decode_b64", "kda_decode_b64_bounded_gate", "kda_verify_b32_t4",
+        for name in ("kda_decode_b8_34layers", "kda_decode_b64", "kda_decode_b64_bounded_gate",
+                     "kda_verify_b32_t4",
                      "kda_verify_b32_t4_outputs_only", "kda_commit_b32_t4", "gdn_prefill_b4_t4096",
                      "kda_prefill_b4_t4096", "kda_layer_decode_b1", "kda_layer_decode_b64"):
             if name == main.name:
                 continue
             w = make_workload(name, device)
             k = args.aux_steps if name not in PREFILL_WORKLOADS else max(3, args.aux_steps // 10)
+            w.capture(sorted({i % getattr(w, "tokens", 1) for i in range(3 + k)}))
             wms = time_steps(w.step, 3, k, flush) / k
             extra[name] = workload_entry(w, wms, peaks)
             del w
@@ -800,7 +809,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(list(synth.WORKLOADS) + list(EXTRA_WORKLOADS) +
-                                   list(LAYER_WORKLOADS)))
+                                   list(LAYER_WORKLOADS) + list(MIDBATCH_WORKLOADS)))
     ap.add_argument("--aux-steps", type=int, default=100)
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-workloads", action="store_true")

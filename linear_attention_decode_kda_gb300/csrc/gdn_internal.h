@@ -49,7 +49,7 @@ bool plan_wstep(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
 cudaError_t launch_wstep(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream);
 
 // Persistent TMA-pipelined kernel (gdn_stream.cu): d = 128, ungrouped heads,
-// at least two (sequence, head) units per SM.
+// more than 64 (sequence, head) units.
 bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan);
 // True when every buffer meets the streaming kernel's 16-byte chunk rules.
 bool stream_eligible(const StepArgs &a);

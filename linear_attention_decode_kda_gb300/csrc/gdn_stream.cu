@@ -461,7 +461,12 @@ bool stream_eligible(const StepArgs &a)
 bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
 {
     const long units = static_cast<long>(B) * H_v;
-    if (D != SD || group != 1 || units < 2L * num_sms || units >= (1L << 24)) return false;
+    // From 65 units the state staged by TMA beats the register-resident slab and
+    // warp-column kernels on the 34-layer chain (us a launch, L2 flushed per step;
+    // B3 H32: 5.55 against 9.29, B4: 5.61 against 9.53, B8: 8.93 against 18.75); at
+    // 64 units (B2 H32) the two-slab kernel stays ahead, 5.17 against 5.37.
+    (void)num_sms;
+    if (D != SD || group != 1 || units <= 64 || units >= (1L << 24)) return false;
     plan->kind = StepPlan::kStream;
     plan->D = SD;
     plan->W = SD;

@@ -209,12 +209,13 @@ def test_variant_choice(lib):
 @pytest.mark.parametrize("B,H_qk,H_v,want", [
     (1, 32, 32, "step<128,16>"),     # below 64 units: the 8-slab plan
     (2, 32, 32, "step<128,64>"),     # 64 to 127 units: two slabs a head
-    (3, 32, 32, "step<128,64>"),
+    (3, 32, 32, "stream<128>"),
     (3, 8, 16, "step<128,32>"),      # 48 grouped units: slabs x group within a cluster of 8
-    (4, 32, 32, "wstep<128,64>"),    # from 128 units: the warp-column kernel, two slabs
-    (9, 32, 32, "wstep<128,64>"),
-    (10, 32, 32, "stream<128>"),     # two units an SM: the streaming kernel
-    (4, 8, 32, "wstep<128,64>"),     # grouped heads never stream
+    (4, 32, 32, "stream<128>"),      # more than 64 ungrouped units: the streaming kernel
+    (9, 32, 32, "stream<128>"),
+    (10, 32, 32, "stream<128>"),
+    (4, 8, 32, "wstep<128,64>"),     # grouped heads never stream: from 128 units the
+    (8, 8, 16, "wstep<128,64>"),     # warp-column kernel, two slabs
     (2, 8, 64, "wstep<128,128>"),    # a group of 8 value heads: whole heads a CTA
 ])
 def test_decode_routing_by_unit_count(lib, B, H_qk, H_v, want):

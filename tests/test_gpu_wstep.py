@@ -46,7 +46,7 @@ def _abi(s):
 
 # (B, H_qk, H_v, variant): two 64-column slabs a head (clusters of 2 x group), and
 # whole heads when a group of 8 value heads shares one qk head
-ROUTES = [(4, 32, 32, "wstep<128,64>"), (8, 8, 16, "wstep<128,64>"),
+ROUTES = [(4, 16, 32, "wstep<128,64>"), (8, 8, 16, "wstep<128,64>"),
           (4, 8, 32, "wstep<128,64>"), (2, 8, 64, "wstep<128,128>")]
 
 
@@ -64,8 +64,10 @@ def test_decode_matches_the_oracle(B, H_qk, H_v, variant, kda):
 
 
 @pytest.mark.parametrize("lb,sig", [(True, False), (False, True), (True, True)])
-def test_gate_variants(lb, sig):
-    shape = _shape(4, 32, 32, kda=True, lb_gate=lb, sigmoid_out=sig)
+@pytest.mark.parametrize("H_qk", [32, 16])
+def test_gate_variants(lb, sig, H_qk):
+    """32 ungrouped heads at B4 stream; pairs of value heads take the warp-column kernel."""
+    shape = _shape(4, H_qk, 32, kda=True, lb_gate=lb, sigmoid_out=sig)
     params, inp, state = _case(shape, 8, seed=32, slow=True)
     y, S, cs = gpu_decode_run(shape, params, inp, state)
     ref = oracle_run(shape, params, inp, state)
