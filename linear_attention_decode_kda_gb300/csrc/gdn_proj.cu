@@ -163,6 +163,128 @@ __global__ void __launch_bounds__(PT) proj_kernel(const __grid_constant__ Args p
     }
 }
 
+__device__ unsigned int g_proj_error;  // bit 0: a bounded mbarrier wait gave up
+
+// ---------------------------------------------------------------- bulk-copy ring
+//
+// The weight stream for a few batch rows (K <= 4096), by bulk copies: one resident
+// CTA an SM, each of its RW warps owning a ring of RING stages of STAGE_B bytes in
+// shared memory.  A warp task is a block of contiguous weight rows of one slot that
+// fills at most a stage (one row of 4096, or 32 rows of 128); warp w takes tasks
+// w, w + W, ... (W warps in all), its lane 0 keeping RING copies in flight, so an SM
+// has up to 192 KB of weights on the way.  The first RING copies of every warp are
+// issued before the dependency wait (weights are read-only), so a launch queued
+// behind another kernel streams its weights into shared memory while that kernel
+// runs.  Lanes multiply from shared memory: tpr lanes a row, one 16-byte piece at a
+// time, all NB batch rows per piece; the sum over a row's lanes is shuffles only.
+constexpr int RW = 8, RING = 3, STAGE_B = 8192;
+constexpr int RING_SMEM = RW * RING * STAGE_B;
+constexpr int RING_MAX_K = STAGE_B / 2;
+
+template <int NB>
+__global__ void __launch_bounds__(RW * 32, 1) proj_ring_kernel(const __grid_constant__ Args p)
+{
+    extern __shared__ __align__(128) unsigned char rsm[];
+    __shared__ __align__(8) uint64_t bar[RW][RING];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gw = static_cast<int>(blockIdx.x) * RW + warp;
+    const int nw = static_cast<int>(gridDim.x) * RW;
+    const int ntask = p.ctas;
+    unsigned char *ring = rsm + static_cast<size_t>(warp) * RING * STAGE_B;
+    if (lane == 0) {
+        for (int i = 0; i < RING; ++i) dev::mbar_init(&bar[warp][i], 1);
+        dev::fence_mbar_init();
+    }
+    __syncwarp();
+
+    // slot, first row and rows of task t
+    auto task = [&](int t, int &si, int &n0, int &nr) {
+        si = 0;
+#pragma unroll
+        for (int k = 1; k < kMaxProjSlots; ++k)
+            if (k < p.nslot && t >= p.s[k].cta0) si = k;
+        const Slot &s = p.s[si];
+        const int rpt = STAGE_B / (2 * s.K);
+        n0 = (t - s.cta0) * rpt;
+        nr = min(rpt, s.N - n0);
+    };
+    auto issue = [&](int k) {  // the warp's k-th task into stage k % RING (lane 0)
+        const int t = gw + k * nw;
+        if (t >= ntask) return;
+        int si, n0, nr;
+        task(t, si, n0, nr);
+        const Slot &s = p.s[si];
+        const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(s.K) * 2u;
+        uint64_t *b = &bar[warp][k % RING];
+        dev::mbar_expect_tx(b, bytes);
+        dev::tma_load_1d(ring + (k % RING) * STAGE_B, s.w + static_cast<size_t>(n0) * s.K, bytes, b);
+    };
+    if (lane == 0)
+        for (int k = 0; k < RING; ++k) issue(k);
+    dev::pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    dev::pdl_launch_dependents();
+
+    bool ok = true;
+    for (int k = 0; gw + k * nw < ntask; ++k) {
+        const int t = gw + k * nw;
+        if (ok) ok = dev::mbar_wait_suspend_bounded(&bar[warp][k % RING], static_cast<uint32_t>((k / RING) & 1));
+        int si, n0, nr;
+        task(t, si, n0, nr);
+        const Slot &s = p.s[si];
+        const int tpr = s.tpr, rpp = 32 / tpr, nk = s.K / 8;
+        const int j = lane % tpr;
+        const unsigned char *stage = ring + (k % RING) * STAGE_B;
+        for (int r0 = 0; r0 < nr; r0 += rpp) {
+            const int r = r0 + lane / tpr;
+            float acc[NB];
+#pragma unroll
+            for (int c = 0; c < NB; ++c) acc[c] = 0.f;
+            if (r < nr) {
+                const uint4 *wrow = reinterpret_cast<const uint4 *>(stage + static_cast<size_t>(r) * s.K * 2);
+#pragma unroll 4
+                for (int kk = j; kk < nk; kk += tpr) {
+                    float w8[8];
+                    unpack8(wrow[kk], w8);
+#pragma unroll
+                    for (int c = 0; c < NB; ++c) {
+                        if (c < p.B) {
+                            float x8[8];
+                            load_x8(s.x, static_cast<size_t>(c) * s.ldx + kk * 8, s.x_bf16, x8);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[c] = fmaf(w8[e], x8[e], acc[c]);
+                        }
+                    }
+                }
+            }
+            for (int off = tpr >> 1; off > 0; off >>= 1)
+#pragma unroll
+                for (int c = 0; c < NB; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], off);
+            if (r < nr && j == 0) {
+#pragma unroll
+                for (int c = 0; c < NB; ++c)
+                    if (c < p.B) s.y[static_cast<size_t>(c) * s.ldy + n0 + r] = acc[c];
+            }
+        }
+        // the stage is read: the copy of the task RING steps ahead may land there
+        dev::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) issue(k + RING);
+    }
+    if (!ok && lane == 0) {
+        // a wait gave up: let every copy still in flight land (bounded) before the CTA
+        // releases its shared memory
+        int ktot = 0;
+        while (gw + ktot * nw < ntask) ++ktot;
+        for (int i = 0; i < RING && i < ktot; ++i) {
+            const int kl = i + RING * ((ktot - 1 - i) / RING);
+            dev::mbar_wait_suspend_bounded(&bar[warp][i], static_cast<uint32_t>((kl / RING) & 1));
+        }
+        atomicOr(&g_proj_error, 1u);
+    }
+}
+
 // ---------------------------------------------------------------- tcgen05 path
 //
 // From 16 batch rows up the products are dense enough for the tensor core: a
@@ -196,7 +318,6 @@ struct TcMaps {
     CUtensorMap w[kMaxProjSlots], x[kMaxProjSlots];
 };
 
-__device__ unsigned int g_proj_error;
 
 // Launches with programmatic dependent launch: the kernels wait for the previous
 // kernel on the stream before they read activations or write outputs.
@@ -492,6 +613,38 @@ cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_
         }
         return slots[0].x_bf16 ? launch_tc<false>(a, slots, tctas, B, stream)
                                : launch_tc<true>(a, slots, tctas, B, stream);
+    }
+    int kmax = 0;
+    for (int i = 0; i < nslot; ++i) kmax = max(kmax, slots[i].K);
+    // narrow rows (the low-rank gate pair, K = rank) stay on the per-row kernel below,
+    // which spreads them over more warps
+    if (kmax >= 1024 && kmax <= RING_MAX_K && B <= 16) {
+        // the bulk-copy ring (every batch row in one pass over the weights): tasks of
+        // STAGE_B / (2 K) rows, one resident CTA an SM
+        static bool ring_attr[64];  // per device; benign race: every writer sets the same value
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!ring_attr[dev]) {
+            for (void (*f)(Args) : {proj_ring_kernel<1>, proj_ring_kernel<2>, proj_ring_kernel<4>,
+                                    proj_ring_kernel<8>, proj_ring_kernel<16>}) {
+                e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, RING_SMEM);
+                if (e != cudaSuccess) return e;
+            }
+            ring_attr[dev] = true;
+        }
+        int tasks = 0;
+        for (int i = 0; i < nslot; ++i) {
+            a.s[i].cta0 = tasks;
+            const int rpt = STAGE_B / (2 * slots[i].K);
+            tasks += (slots[i].N + rpt - 1) / rpt;
+        }
+        a.ctas = tasks;
+        void (*fn)(Args) = B > 8 ? proj_ring_kernel<16> : B > 4 ? proj_ring_kernel<8>
+                         : B > 2 ? proj_ring_kernel<4> : B > 1 ? proj_ring_kernel<2> : proj_ring_kernel<1>;
+        return launch_pdl(fn, dim3(max(1, min(num_sms(), (tasks + RW - 1) / RW))), RW * 32, RING_SMEM,
+                          stream, a);
     }
     a.ctas = ctas;
     a.pf_ctas = prefetch ? min(ctas, num_sms()) : 0;
