@@ -222,6 +222,27 @@ __device__ __forceinline__ void tma_load_1d(void *dst_smem, const void *src_gmem
         : "memory");
 }
 
+// An L2 policy that marks the lines a load brings in as the first to evict: for data
+// read once (weights streamed past the cache), so it does not displace lines that a
+// later kernel will read.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_1d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_1d_hint(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                                 uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // Tiled TMA copies through a tensor map (passed as a __grid_constant__ kernel
 // parameter); the innermost coordinate times the element size is a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, int x, int y,

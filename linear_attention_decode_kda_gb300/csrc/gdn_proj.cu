@@ -41,6 +41,7 @@ struct Args {
     int ksplit;  // tensor-core path: K ranges per output tile (partial sums added atomically)
     int ctas;    // CUDA-core path: CTAs of the launch
     int pf_ctas; // CUDA-core path: the first pf_ctas CTAs ask L2 for every CTA's rows
+    int mr_k;    // warp-MMA path: K of every slot
 };
 
 __device__ __forceinline__ void unpack8(const uint4 r, float (&v)[8])
@@ -186,38 +187,44 @@ __global__ void __launch_bounds__(RW * 32, 1) proj_ring_kernel(const __grid_cons
 {
     extern __shared__ __align__(128) unsigned char rsm[];
     __shared__ __align__(8) uint64_t bar[RW][RING];
+    // The slot table in shared memory: indexed by a run-time slot number, the kernel
+    // parameter would be read through a generic address on every use.
+    __shared__ Slot ss[kMaxProjSlots];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = static_cast<int>(blockIdx.x) * RW + warp;
     const int nw = static_cast<int>(gridDim.x) * RW;
-    const int ntask = p.ctas;
+    const int ntask = p.ctas, nslot = p.nslot, B = p.B;
     unsigned char *ring = rsm + static_cast<size_t>(warp) * RING * STAGE_B;
+    const uint64_t wpol = dev::l2_policy_evict_first();  // weights are read once
+#pragma unroll
+    for (int i = 0; i < kMaxProjSlots; ++i)
+        if (static_cast<int>(threadIdx.x) == i && i < nslot) ss[i] = p.s[i];
     if (lane == 0) {
         for (int i = 0; i < RING; ++i) dev::mbar_init(&bar[warp][i], 1);
         dev::fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
 
     // slot, first row and rows of task t
     auto task = [&](int t, int &si, int &n0, int &nr) {
         si = 0;
-#pragma unroll
-        for (int k = 1; k < kMaxProjSlots; ++k)
-            if (k < p.nslot && t >= p.s[k].cta0) si = k;
-        const Slot &s = p.s[si];
-        const int rpt = STAGE_B / (2 * s.K);
-        n0 = (t - s.cta0) * rpt;
-        nr = min(rpt, s.N - n0);
+        for (int k = 1; k < nslot; ++k)
+            if (t >= ss[k].cta0) si = k;
+        const int K = ss[si].K, rpt = STAGE_B / (2 * K);
+        n0 = (t - ss[si].cta0) * rpt;
+        nr = min(rpt, ss[si].N - n0);
     };
     auto issue = [&](int k) {  // the warp's k-th task into stage k % RING (lane 0)
         const int t = gw + k * nw;
         if (t >= ntask) return;
         int si, n0, nr;
         task(t, si, n0, nr);
-        const Slot &s = p.s[si];
-        const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(s.K) * 2u;
+        const int K = ss[si].K;
+        const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(K) * 2u;
         uint64_t *b = &bar[warp][k % RING];
         dev::mbar_expect_tx(b, bytes);
-        dev::tma_load_1d(ring + (k % RING) * STAGE_B, s.w + static_cast<size_t>(n0) * s.K, bytes, b);
+        dev::tma_load_1d_hint(ring + (k % RING) * STAGE_B, ss[si].w + static_cast<size_t>(n0) * K, bytes, b,
+                              wpol);
     };
     if (lane == 0)
         for (int k = 0; k < RING; ++k) issue(k);
@@ -232,9 +239,11 @@ __global__ void __launch_bounds__(RW * 32, 1) proj_ring_kernel(const __grid_cons
         if (ok) ok = dev::mbar_wait_suspend_bounded(&bar[warp][k % RING], static_cast<uint32_t>((k / RING) & 1));
         int si, n0, nr;
         task(t, si, n0, nr);
-        const Slot &s = p.s[si];
-        const int tpr = s.tpr, rpp = 32 / tpr, nk = s.K / 8;
-        const int j = lane % tpr;
+        const int K = ss[si].K, tpr = ss[si].tpr, ldx = ss[si].ldx, ldy = ss[si].ldy;
+        const bool xb = ss[si].x_bf16 != 0;
+        const void *x = ss[si].x;
+        float *y = ss[si].y + n0;
+        const int rpp = 32 / tpr, nk = K / 8, j = lane % tpr;
         const unsigned char *stage = ring + (k % RING) * STAGE_B;
         for (int r0 = 0; r0 < nr; r0 += rpp) {
             const int r = r0 + lane / tpr;
@@ -242,16 +251,16 @@ __global__ void __launch_bounds__(RW * 32, 1) proj_ring_kernel(const __grid_cons
 #pragma unroll
             for (int c = 0; c < NB; ++c) acc[c] = 0.f;
             if (r < nr) {
-                const uint4 *wrow = reinterpret_cast<const uint4 *>(stage + static_cast<size_t>(r) * s.K * 2);
+                const uint4 *wrow = reinterpret_cast<const uint4 *>(stage + static_cast<size_t>(r) * K * 2);
 #pragma unroll 4
                 for (int kk = j; kk < nk; kk += tpr) {
                     float w8[8];
                     unpack8(wrow[kk], w8);
 #pragma unroll
                     for (int c = 0; c < NB; ++c) {
-                        if (c < p.B) {
+                        if (c < B) {
                             float x8[8];
-                            load_x8(s.x, static_cast<size_t>(c) * s.ldx + kk * 8, s.x_bf16, x8);
+                            load_x8(x, static_cast<size_t>(c) * ldx + kk * 8, xb, x8);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) acc[c] = fmaf(w8[e], x8[e], acc[c]);
                         }
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(RW * 32, 1) proj_ring_kernel(const __grid_cons
             if (r < nr && j == 0) {
 #pragma unroll
                 for (int c = 0; c < NB; ++c)
-                    if (c < p.B) s.y[static_cast<size_t>(c) * s.ldy + n0 + r] = acc[c];
+                    if (c < B) y[static_cast<size_t>(c) * ldy + r] = acc[c];
             }
         }
         // the stage is read: the copy of the task RING steps ahead may land there
@@ -282,6 +291,173 @@ __global__ void __launch_bounds__(RW * 32, 1) proj_ring_kernel(const __grid_cons
             dev::mbar_wait_suspend_bounded(&bar[warp][i], static_cast<uint32_t>((kl / RING) & 1));
         }
         atomicOr(&g_proj_error, 1u);
+    }
+}
+
+// ---------------------------------------------------------------- warp-MMA GEMV
+//
+// Up to 8 batch rows of bf16 activations (4 of fp32): the products run on the
+// warp-level tensor-core MMA (m16n8k16, bf16 operands, fp32 accumulation).  On CUDA
+// cores the weight stream is limited by instructions (each 16-byte piece is unpacked to
+// fp32 and multiplied element by element); here one 16-byte load a lane feeds two MMAs.
+// A is the activations: batch row g in row g and, with fp32 activations, the bf16
+// remainder x - bf16(x) of row g in row g + 8 (each output adds the two rows: about 16
+// significant bits of x).  B is eight weight rows: lane (g, j) loads elements
+// 8 j ... 8 j + 7 of a 32-column unit of row g and hands them to two MMAs as its
+// fragments; the activation fragments follow the same order of k, and a dot product
+// does not depend on the order of its terms.
+//
+// A CTA (16 warps, one an SM) takes tasks of 8 weight rows; its warps split K into
+// units of 32 columns and add their partial sums in shared memory in a fixed order.
+// Each warp loads a task's weights in one round of 16-byte loads (up to 8 a lane) and
+// issues the next task's before it multiplies, so an SM has two tasks in flight; the
+// first task's loads go out before the dependency wait (the weights are read-only).
+constexpr int MW = 16;                   // warps a CTA
+constexpr int MU = 8;                    // 32-column units a warp, at most, per task
+constexpr int MMA_MAX_K = MW * MU * 32;  // 4096
+constexpr int MXS_MAX = 65536;           // activation fragments in shared memory
+
+__device__ __forceinline__ uint4 ldg_stream(const void *ptr, uint64_t policy)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "l"(policy));
+    return v;
+}
+
+// d += A (16 x 16 bf16, row fragments a) * B (16 x 8 bf16, column fragments b0 b1)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// bf16 pair (u, v) and the pair of remainders (u - bf16(u), v - bf16(v)), the first
+// element in the low half
+__device__ __forceinline__ void split_pair(float u, float v, uint32_t &hi, uint32_t &lo)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(u, v);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(u - hf.x, v - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(MW * 32, 1) proj_mma_kernel(const __grid_constant__ Args p)
+{
+    extern __shared__ __align__(16) unsigned char msm[];  // activation fragments
+    __shared__ Slot ss[kMaxProjSlots];
+    __shared__ float red[2][MW][64];  // a warp's partial outputs: batch row g, task row n at 8 g + n
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, j = lane & 3;
+    const int ntile = p.ctas, nslot = p.nslot, B = p.B, K = p.mr_k, nl = 4 * B;
+    const int nu = K / 32, u0 = warp * nu / MW, u1 = (warp + 1) * nu / MW;  // this warp's units
+    const uint64_t pol = dev::l2_policy_evict_first();  // weights are read once
+#pragma unroll
+    for (int i = 0; i < kMaxProjSlots; ++i)
+        if (static_cast<int>(threadIdx.x) == i && i < nslot) ss[i] = p.s[i];
+    __syncthreads();
+
+    // slot, first row and rows of task t
+    auto task = [&](int t, int &si, int &r0, int &nr) {
+        si = 0;
+        for (int k = 1; k < nslot; ++k)
+            if (t >= ss[k].cta0) si = k;
+        r0 = (t - ss[si].cta0) * 8;
+        nr = min(8, ss[si].N - r0);
+    };
+    // this lane's weights of task t: row r0 + g, elements 8 j ... 8 j + 7 of each unit
+    auto load = [&](int t, uint4 (&w)[MU]) {
+        int si, r0, nr;
+        task(t, si, r0, nr);
+        const __nv_bfloat16 *row = ss[si].w + static_cast<size_t>(r0 + (g < nr ? g : 0)) * K + j * 8;
+#pragma unroll
+        for (int u = 0; u < MU; ++u)
+            w[u] = (u0 + u < u1 && g < nr) ? ldg_stream(row + (u0 + u) * 32, pol) : make_uint4(0u, 0u, 0u, 0u);
+    };
+
+    uint4 wa[MU], wb[MU];
+    int t = blockIdx.x;
+    load(t, wa);
+    dev::pdl_wait();
+    // Dependents launch only once this grid has passed its own dependency wait, so a
+    // dependent's pre-wait reads overlap this kernel alone, never an earlier one.
+    dev::pdl_launch_dependents();
+
+    // Activation fragments, unit major: entry (u, l) for lane l < 4B holds row g = l / 4,
+    // elements 32 u + 8 (l % 4) ... + 7 (fp32 activations: the bf16 pairs, then their
+    // remainders).
+    uint4 *xs4 = reinterpret_cast<uint4 *>(msm);
+    {
+        const void *x = ss[0].x;
+        const int ldx = ss[0].ldx;
+        for (int i = threadIdx.x; i < nu * nl; i += MW * 32) {
+            const int u = i / nl, l = i - u * nl;
+            const size_t off = static_cast<size_t>(l >> 2) * ldx + u * 32 + (l & 3) * 8;
+            if (SPLIT) {
+                const float4 e0 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + off);
+                const float4 e1 = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + off + 4);
+                uint4 hi, lo;
+                split_pair(e0.x, e0.y, hi.x, lo.x);
+                split_pair(e0.z, e0.w, hi.y, lo.y);
+                split_pair(e1.x, e1.y, hi.z, lo.z);
+                split_pair(e1.z, e1.w, hi.w, lo.w);
+                xs4[2 * i] = hi;
+                xs4[2 * i + 1] = lo;
+            } else {
+                xs4[i] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(x) + off);
+            }
+        }
+    }
+    __syncthreads();
+
+    for (int par = 0; t < ntile; t += gridDim.x, par ^= 1) {
+        if (t + static_cast<int>(gridDim.x) < ntile) load(t + gridDim.x, wb);  // in flight meanwhile
+        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int u = 0; u < MU; ++u) {
+            if (u0 + u < u1) {
+                uint32_t a[4] = {0u, 0u, 0u, 0u}, c[4] = {0u, 0u, 0u, 0u};
+                if (lane < nl) {
+                    const int e = (u0 + u) * nl + lane;
+                    if (SPLIT) {
+                        const uint4 hi = xs4[2 * e], lo = xs4[2 * e + 1];
+                        a[0] = hi.x; a[1] = lo.x; a[2] = hi.y; a[3] = lo.y;
+                        c[0] = hi.z; c[1] = lo.z; c[2] = hi.w; c[3] = lo.w;
+                    } else {
+                        const uint4 v = xs4[e];
+                        a[0] = v.x; a[2] = v.y;
+                        c[0] = v.z; c[2] = v.w;
+                    }
+                }
+                mma_bf16_16816(d[0], a, wa[u].x, wa[u].y);
+                mma_bf16_16816(d[1], c, wa[u].z, wa[u].w);
+            }
+        }
+        // lane (g, j): batch row g, task rows 2 j and 2 j + 1 (MMA rows g + 8 carry the
+        // remainders' share, zero for bf16 activations)
+        if (g < B) {
+            red[par][warp][g * 8 + 2 * j] = (d[0][0] + d[1][0]) + (d[0][2] + d[1][2]);
+            red[par][warp][g * 8 + 2 * j + 1] = (d[0][1] + d[1][1]) + (d[0][3] + d[1][3]);
+        }
+        __syncthreads();
+        if (static_cast<int>(threadIdx.x) < 8 * B) {
+            int si, r0, nr;
+            task(t, si, r0, nr);
+            const int gb = threadIdx.x >> 3, n = threadIdx.x & 7;
+            if (n < nr) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < MW; ++w) v += red[par][w][gb * 8 + n];
+                ss[si].y[static_cast<size_t>(gb) * ss[si].ldy + r0 + n] = v;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < MU; ++u) wa[u] = wb[u];
     }
 }
 
@@ -613,6 +789,36 @@ cudaError_t launch_proj(const ProjSlotDesc *slots, int nslot, int B, cudaStream_
         }
         return slots[0].x_bf16 ? launch_tc<false>(a, slots, tctas, B, stream)
                                : launch_tc<true>(a, slots, tctas, B, stream);
+    }
+    // the warp-MMA GEMV: every slot reads the same activations (up to 8 bf16 rows, 4
+    // fp32) against K columns, a multiple of 32 up to 4096
+    bool mma_ok = B <= (slots[0].x_bf16 ? 8 : 4) && slots[0].K % 32 == 0 && slots[0].K <= MMA_MAX_K;
+    for (int i = 1; i < nslot; ++i)
+        mma_ok = mma_ok && slots[i].K == slots[0].K && slots[i].x == slots[0].x &&
+                 slots[i].ldx == slots[0].ldx && slots[i].x_bf16 == slots[0].x_bf16;
+    const int xs_bytes = B * slots[0].K * (slots[0].x_bf16 ? 2 : 4);
+    if (mma_ok && xs_bytes <= MXS_MAX) {
+        static bool mma_attr[64];  // per device; benign race: every writer sets the same value
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!mma_attr[dev]) {
+            for (void (*f)(Args) : {proj_mma_kernel<false>, proj_mma_kernel<true>}) {
+                e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, MXS_MAX);
+                if (e != cudaSuccess) return e;
+            }
+            mma_attr[dev] = true;
+        }
+        int tasks = 0;
+        for (int i = 0; i < nslot; ++i) {
+            a.s[i].cta0 = tasks;
+            tasks += (slots[i].N + 7) / 8;
+        }
+        a.ctas = tasks;
+        a.mr_k = slots[0].K;
+        return launch_pdl(slots[0].x_bf16 ? proj_mma_kernel<false> : proj_mma_kernel<true>,
+                          dim3(max(1, min(num_sms(), tasks))), MW * 32, xs_bytes, stream, a);
     }
     int kmax = 0;
     for (int i = 0; i < nslot; ++i) kmax = max(kmax, slots[i].K);

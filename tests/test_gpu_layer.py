@@ -55,6 +55,7 @@ def _run(shape, d_model, rank, seed):
     assert_close(x_out, ref["x_out"], DECODE_TOL, "x_out")
     assert_close(case.state, ref["state"], DECODE_TOL, "state")
     assert_close(case.conv_state, ref["conv_state"], ROW_TOL, "conv_state")
+    return x_out, case.out, case.state, case.qkv
 
 
 @pytest.mark.parametrize("B", [1, 3, 9])
@@ -83,3 +84,31 @@ def test_layer_decode_b64_h32_d4096():
     """The bench's batched layer: 64 sequences, 32 heads, d_model 4096, rank 128."""
     shape = synth.Shape(B=64, T=1, H_qk=32, H_v=32, d_k=128, d_v=128, kda=True)
     _run(shape, 4096, 128, seed=71)
+
+
+@pytest.mark.parametrize("B,d_model,H", [(1, 4096, 32), (2, 1024, 8), (3, 1536, 12),
+                                          (8, 2048, 8), (4, 2304, 8)])
+def test_layer_decode_warp_mma(B, d_model, H):
+    """K a multiple of 32 up to 4096 with up to 8 bf16 activation rows (the
+    in-projection) or 4 fp32 rows (the output projection, each split into a bf16 value
+    and a bf16 remainder): warp-level MMA.  B = 8 keeps the output projection on the
+    CUDA-core ring."""
+    shape = synth.Shape(B=B, T=1, H_qk=H, H_v=H, d_k=128, d_v=128, kda=True)
+    _run(shape, d_model, 64, seed=90 + B)
+
+
+@pytest.mark.parametrize("B,d_model,H", [(5, 3072, 8), (15, 2048, 16), (12, 1024, 8)])
+def test_layer_decode_bulk_copy_ring(B, d_model, H):
+    """Rows of 1024 to 4096 past the warp-MMA's batch (fp32 activations from 5 rows,
+    bf16 from 9) stream through per-warp rings of bulk copies into CUDA-core FMAs."""
+    shape = synth.Shape(B=B, T=1, H_qk=H, H_v=H, d_k=128, d_v=128, kda=True)
+    _run(shape, d_model, 64, seed=100 + B)
+
+
+def test_layer_decode_repeat_is_bitwise():
+    """Fixed reduction orders: the same inputs give the same bits."""
+    shape = synth.Shape(B=2, T=1, H_qk=8, H_v=8, d_k=128, d_v=128, kda=True)
+    a = _run(shape, 1024, 64, seed=110)
+    b = _run(shape, 1024, 64, seed=110)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
