@@ -320,7 +320,7 @@ constexpr int MXS_MAX = 65536;           // activation fragments in shared memor
 __device__ __forceinline__ uint4 ldg_stream(const void *ptr, uint64_t policy)
 {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(ptr), "l"(policy));
     return v;
