@@ -254,10 +254,11 @@ typedef struct {
 
 /*
  * One decode step of a whole KDA layer for B sequences (T = 1): the
- * projections around the step fused into four launches.  From the layer input
- * x ([B][d_model] bf16, 16-byte aligned):
+ * projections around the step fused into three or four launches.  From the
+ * layer input x ([B][d_model] bf16, 16-byte aligned):
  *   qkv = x w_qkv^T, f_a = x w_fa^T, g_a = x w_ga^T, beta = x w_beta^T   (one launch)
- *   f = f_a w_fb^T, z = g_a w_gb^T                                       (one launch)
+ *   f = f_a w_fb^T, z = g_a w_gb^T              (one launch, or inside the step when
+ *                                                the step runs on the column-slab kernel)
  *   the step of gdn_decode_step on those rows                            (the step)
  *   x_out = y w_o^T                                                      (one launch)
  * "Thirty tiny kernels per layer" (the decode budget: these projections are
@@ -270,7 +271,7 @@ typedef struct {
  * workspace holds gdn_layer_workspace_bytes bytes (the low-rank rows),
  * 16-byte aligned.  x_out is [B][d_model] fp32.
  *
- * The four launches use programmatic dependent launch whatever shape->flags
+ * The launches use programmatic dependent launch whatever shape->flags
  * holds: each kernel reads activations and writes its outputs only after the
  * previous kernel on the stream has completed, and before that touches nothing
  * but read-only weights (asked into L2) and, for the step, its own state,

@@ -345,10 +345,24 @@ gdn_status_t gdn_layer_decode(const gdn_shape_t *s, const gdn_layer_weights_t *w
         if (!gdn::proj_slot_ok(d)) return GDN_ERR_ALIGN;
     if (!gdn::proj_slot_ok(out[0])) return GDN_ERR_ALIGN;
     if (gdn::launch_proj(in, 4, B, st, false) != cudaSuccess) return GDN_ERR_CUDA;
-    if (gdn::launch_proj(gate, 2, B, st, true) != cudaSuccess) return GDN_ERR_CUDA;
     gdn::StepArgs a = step_args(s, t);
     a.state_out = t->state;
     a.conv_out = t->conv_state;
+    // On the column-slab kernel the low-rank gates' second products run inside the
+    // step (each CTA from its head's W_fb rows and its columns' W_gb rows), which saves
+    // a launch and its dependency on the critical path; otherwise the gate pair is a
+    // projection launch of its own.
+    if (plan.kind == gdn::StepPlan::kSlab &&
+        gdn::slab_gate_smem(plan.D, plan.W, R) <= gdn::kSlabGateSmemMax) {
+        a.gate_lr = lr;
+        a.w_fb = w->w_fb;
+        a.w_gb = w->w_gb;
+        a.gate_rank = R;
+        a.gate_f = f;
+        a.gate_z = z;
+    } else if (gdn::launch_proj(gate, 2, B, st, true) != cudaSuccess) {
+        return GDN_ERR_CUDA;
+    }
     // The step overlaps its prologue with the projections before it, which write only
     // the rows it reads after its dependency wait.
     gdn_shape_t sp = *s;

@@ -222,6 +222,19 @@ __device__ __forceinline__ void tma_load_1d(void *dst_smem, const void *src_gmem
         : "memory");
 }
 
+// 16 bytes global -> shared without registers (both 16-byte aligned); completes at
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src_gmem)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // An L2 policy that marks the lines a load brings in as the first to evict: for data
 // read once (weights streamed past the cache), so it does not displace lines that a
 // later kernel will read.

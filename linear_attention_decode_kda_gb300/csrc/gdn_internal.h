@@ -27,7 +27,28 @@ struct StepArgs {
     int sig_gate;                // output gate sigmoid(z) instead of silu(z)
     int in_bf16, out_bf16;
     float q_scale, eps_l2, eps_norm;
+    // Low-rank gates inside the column-slab kernel (a layer's decode, T = 1, per-channel
+    // decay): f[b,h,:] = W_fb[h D .. h D + D) lr[b, 0:R] and z[b,h,:] likewise from W_gb
+    // and lr[b, R:2R]; lr is [B][2R] fp32, W_fb and W_gb [H_v D][R] bf16 (16-byte
+    // aligned, R a multiple of 8).  NULL: f and z are read as rows.  Only the slab
+    // kernel takes them (slab_gate_smem bytes of dynamic shared memory): each slab
+    // computes f for its own W key channels and hands them to the head's other slabs
+    // through the cluster.
+    const float *gate_lr;
+    const void *w_fb, *w_gb;
+    int gate_rank;
+    float *gate_f, *gate_z;  // the in-kernel gates' f and z also stored as rows (fp32), or NULL
 };
+
+// Dynamic shared memory of the slab kernel's in-kernel gates: the W_fb rows of the
+// slab's key channels and the W_gb rows of its value columns (each padded by 16 bytes),
+// and the lr row.
+inline int slab_gate_smem(int D, int W, int R)
+{
+    (void)D;
+    return 2 * W * (2 * R + 16) + 8 * R;
+}
+constexpr int kSlabGateSmemMax = 48 * 1024;
 
 // One launch configuration of the step kernels.
 struct StepPlan {

@@ -46,6 +46,26 @@ __device__ unsigned int g_step_error;  // bit 0: a bounded mbarrier wait gave up
 // of a warp taking alternate lines.  Nothing comes back to the thread, so this may
 // run before the dependency wait on rows the previous kernel is still writing: L2 is
 // the point of coherence, and the loads after the wait read the lines as written.
+// 8 bf16 weights (16 bytes of shared memory) times 8 fp32 values (shared memory)
+__device__ __forceinline__ float dot8_bf16(const unsigned char *w16, const float *x8)
+{
+    const uint4 w = *reinterpret_cast<const uint4 *>(w16);
+    const float4 xa = *reinterpret_cast<const float4 *>(x8);
+    const float4 xb = *reinterpret_cast<const float4 *>(x8 + 4);
+    const float2 w0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+    const float2 w1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+    const float2 w2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.z));
+    const float2 w3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.w));
+    float acc = w0.x * xa.x;
+    acc = fmaf(w0.y, xa.y, acc);
+    acc = fmaf(w1.x, xa.z, acc);
+    acc = fmaf(w1.y, xa.w, acc);
+    acc = fmaf(w2.x, xb.x, acc);
+    acc = fmaf(w2.y, xb.y, acc);
+    acc = fmaf(w3.x, xb.z, acc);
+    return fmaf(w3.y, xb.w, acc);
+}
+
 __device__ __forceinline__ void prefetch_l2_lines(const void *p, size_t bytes, int lane)
 {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
@@ -90,6 +110,12 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     __shared__ float rms_slot[2][NSLAB];
     __shared__ __align__(8) uint64_t rms_bar[2];  // completed by the slabs' pushes of token parity
     __shared__ float beta_s;
+    __shared__ float z_s[W];
+    __shared__ float f_s[D];                // in-kernel gates: the head's f
+    __shared__ __align__(8) uint64_t f_bar;  // completed by the slabs' pushes of their f share
+    // in-kernel gates (a.gate_lr): the W_fb rows of the slab's W key channels, the W_gb
+    // rows of its W value columns (each 2R + 16 bytes), then the lr row of the sequence
+    extern __shared__ __align__(16) unsigned char gsm[];
 
     uint32_t rank0 = 0;  // cluster rank of slab 0 of this head
     if (clustered) {
@@ -97,6 +123,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         if (tid == 0) {
             mbar_init(&rms_bar[0], 1);
             mbar_init(&rms_bar[1], 1);
+            mbar_init(&f_bar, 1);
             fence_mbar_init();
         }
     }
@@ -152,6 +179,20 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     }
     const float dtb_head = a.kda ? 0.0f : a.dt_bias[h];
 
+    // In-kernel gates: the weight rows they need go to shared memory now (read-only).
+    const bool gates = a.gate_lr != nullptr;
+    const int GR = a.gate_rank, GS = 2 * GR + 16;
+    if (gates) {
+        const int cpr = GR / 8;  // 16-byte pieces a row
+        for (int i = tid; i < 2 * W * cpr; i += NT) {
+            const int r = i / cpr, c = i - r * cpr;
+            const bool fb = r < W;
+            const size_t grow = static_cast<size_t>(h) * D + slab * W + (fb ? r : r - W);
+            cp_async16(gsm + r * GS + c * 16,
+                       static_cast<const __nv_bfloat16 *>(fb ? a.w_fb : a.w_gb) + grow * GR + c * 8);
+        }
+    }
+
     // The rows of the first tokens' inputs are asked into L2 now, so that the loads
     // after the wait find them there (a warp per input segment).
     {
@@ -168,10 +209,15 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             case 1: p = qkv + (row + static_cast<size_t>(a.H_qk + hq) * D) * esz; n = D; break;
             case 2: p = qkv + (row + 2 * static_cast<size_t>(a.H_qk) * D + h * D + slab * W) * esz; n = W; break;
             case 3:
+                if (gates) break;
                 p = static_cast<const char *>(a.f) + (a.kda ? bth * D : bth) * esz;
                 n = a.kda ? D : 1;
                 break;
-            case 4: p = static_cast<const char *>(a.z) + (bth * D + slab * W) * esz; n = W; break;
+            case 4:
+                if (gates) break;
+                p = static_cast<const char *>(a.z) + (bth * D + slab * W) * esz;
+                n = W;
+                break;
             default: p = static_cast<const char *>(a.beta) + bth * esz; n = 1; break;
             }
             prefetch_l2_lines(p, n * esz, lane);
@@ -200,7 +246,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             if (i < D) {
                 in.xq[m] = ld_in(a.qkv, row + hq * D + i, a.in_bf16);
                 in.xk[m] = ld_in(a.qkv, row + a.H_qk * D + hq * D + i, a.in_bf16);
-                in.fq[m] = a.kda ? ld_in(a.f, bth * D + i, a.in_bf16) : 0.0f;
+                in.fq[m] = a.kda && !gates ? ld_in(a.f, bth * D + i, a.in_bf16) : 0.0f;
             }
         }
 #pragma unroll
@@ -208,7 +254,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
             const int j = tv + m * NT;
             if (j < W) in.xv[m] = ld_in(a.qkv, row + 2 * a.H_qk * D + h * D + slab * W + j, a.in_bf16);
         }
-        if (rg == 0) {
+        if (rg == 0 && !gates) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) in.z[c] = ld_in(a.z, bth * D + col0 + c, a.in_bf16);
         }
@@ -223,6 +269,56 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     const int Tb = a.accepted ? min(max(a.accepted[b], 0), a.T) : a.T;
     if (Tb > 0) load_token(0, cur);
     if (clustered) cluster_wait_acquire();  // every CTA's barriers and window reads
+    if (gates) {
+        // The slab's 2W outputs: f of key channels slab W + o (o < W), which every slab
+        // of the head needs for its decay, and z of its own value columns (o >= W); NT /
+        // (2W) threads an output, 16-byte pieces of the rank taken round robin.
+        float *lr_s = reinterpret_cast<float *>(gsm + 2 * W * GS);
+        const size_t bth0 = static_cast<size_t>(b) * a.Ts * a.H_v + h;  // token 0
+        for (int i = tid; i < 2 * GR; i += NT) lr_s[i] = a.gate_lr[static_cast<size_t>(b) * 2 * GR + i];
+        cp_async_wait_all();
+        __syncthreads();
+        constexpr int PARTS = NT / (2 * W);
+        static_assert(PARTS >= 1 && 32 % PARTS == 0, "gate output split");
+        const int o = tid / PARTS, part = tid % PARTS;
+        const float *x = lr_s + (o < W ? 0 : GR);
+        float g0 = 0.f, g1 = 0.f;
+        int c = part;
+        for (; c + PARTS < GR / 8; c += 2 * PARTS) {
+            g0 += dot8_bf16(gsm + o * GS + c * 16, x + c * 8);
+            g1 += dot8_bf16(gsm + o * GS + (c + PARTS) * 16, x + (c + PARTS) * 8);
+        }
+        if (c < GR / 8) g0 += dot8_bf16(gsm + o * GS + c * 16, x + c * 8);
+        float gv = g0 + g1;
+#pragma unroll
+        for (int off = PARTS >> 1; off > 0; off >>= 1) gv += __shfl_xor_sync(0xffffffffu, gv, off);
+        if (NSLAB > 1 && tid == 0) mbar_expect_tx(&f_bar, D * 4);
+        if (part == 0) {
+            if (o < W) {
+                const int ch = slab * W + o;
+                if (NSLAB > 1) {
+                    for (int d = 0; d < NSLAB; ++d) st_async_remote(&f_s[ch], rank0 + d, gv, &f_bar);
+                } else {
+                    f_s[ch] = gv;
+                }
+                if (a.gate_f) a.gate_f[bth0 * D + ch] = gv;
+            } else {
+                z_s[o - W] = gv;
+                if (a.gate_z) a.gate_z[bth0 * D + slab * W + (o - W)] = gv;
+            }
+        }
+        __syncthreads();
+        if (NSLAB > 1) ok &= mbar_wait_cluster_bounded(&f_bar, 0u);
+#pragma unroll
+        for (int m = 0; m < CQ; ++m) {
+            const int i = tid + m * NT;
+            if (i < D) cur.fq[m] = f_s[i];
+        }
+        if (rg == 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) cur.z[c4] = z_s[4 * cg + c4];
+        }
+    }
 
 #pragma unroll 1
     for (int t = 0; t < Tb; ++t) {
@@ -859,6 +955,14 @@ cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaS
     cfg.gridDim = dim3(plan.nslab, a.H_v, a.B);
     cfg.blockDim = dim3(plan.threads, 1, 1);
     cfg.dynamicSmemBytes = 0;
+    if (a.gate_lr) {
+        const int gs = slab_gate_smem(plan.D, plan.W, a.gate_rank);
+        if (a.T != 1 || !a.kda || a.gate_rank <= 0 || a.gate_rank % 8 || gs > kSlabGateSmemMax ||
+            !a.w_fb || !a.w_gb || (reinterpret_cast<uintptr_t>(a.w_fb) & 15u) ||
+            (reinterpret_cast<uintptr_t>(a.w_gb) & 15u))
+            return cudaErrorInvalidValue;
+        cfg.dynamicSmemBytes = static_cast<size_t>(gs);
+    }
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -925,6 +1029,7 @@ bool plan_wstep(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
 
 cudaError_t launch_wstep(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
 {
+    if (a.gate_lr) return cudaErrorInvalidValue;  // in-kernel gates: slab kernel only
     const WVariant *v = find_wvariant(plan.W);
     if (!v || plan.D != WD) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

@@ -480,6 +480,7 @@ bool plan_stream(int D, int B, int H_v, int group, int num_sms, StepPlan *plan)
 
 cudaError_t launch_stream(const StepPlan &plan, const StepArgs &a, bool pdl, cudaStream_t stream)
 {
+    if (a.gate_lr) return cudaErrorInvalidValue;  // in-kernel gates: slab kernel only
     const int es = a.in_bf16 ? 2 : 4;
     const CUtensorMapDataType ty = a.in_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
