@@ -460,7 +460,10 @@ class LayerDecode(Workload):
         self.tensors = self.case.abi_tensors()
         self.kernel = "proj + " + (gdn.gdn_kernel_variant(self.abi_shape, gdn.OP_DECODE) or "?")
         self.launches_per_step = 1
-        self.kernels_per_launch = 4
+        # in-projection, step, output projection; the gate pair is a launch of its own
+        # unless the step runs on the column-slab kernel, which computes the gates itself
+        step_kernel = gdn.gdn_kernel_variant(self.abi_shape, gdn.OP_DECODE) or ""
+        self.kernels_per_launch = 3 if step_kernel.startswith("step<") else 4
         self.units_per_step = s.B
         wbytes = sum(int(v.numel()) * 2 for v in self.w.values())
         self.weight_bytes = wbytes

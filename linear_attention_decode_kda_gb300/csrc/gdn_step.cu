@@ -82,7 +82,9 @@ struct TokenIn {
     float beta, fh;
 };
 
-template <int D, int W, int NT>
+// GATES: the low-rank gates computed in the kernel (StepArgs::gate_lr), a separate
+// instantiation so the plain step keeps its own code.
+template <int D, int W, int NT, bool GATES>
 __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kernel(const StepArgs a)
 {
     constexpr int TPR = W / 4;          // threads per state row, one float4 each
@@ -110,8 +112,8 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     __shared__ float rms_slot[2][NSLAB];
     __shared__ __align__(8) uint64_t rms_bar[2];  // completed by the slabs' pushes of token parity
     __shared__ float beta_s;
-    __shared__ float z_s[W];
-    __shared__ float f_s[D];                // in-kernel gates: the head's f
+    __shared__ float z_s[GATES ? W : 1];
+    __shared__ float f_s[GATES ? D : 1];     // in-kernel gates: the head's f
     __shared__ __align__(8) uint64_t f_bar;  // completed by the slabs' pushes of their f share
     // in-kernel gates (a.gate_lr): the W_fb rows of the slab's W key channels, the W_gb
     // rows of its W value columns (each 2R + 16 bytes), then the lr row of the sequence
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
         if (tid == 0) {
             mbar_init(&rms_bar[0], 1);
             mbar_init(&rms_bar[1], 1);
-            mbar_init(&f_bar, 1);
+            if (GATES) mbar_init(&f_bar, 1);
             fence_mbar_init();
         }
     }
@@ -180,9 +182,9 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     const float dtb_head = a.kda ? 0.0f : a.dt_bias[h];
 
     // In-kernel gates: the weight rows they need go to shared memory now (read-only).
-    const bool gates = a.gate_lr != nullptr;
+    constexpr bool gates = GATES;
     const int GR = a.gate_rank, GS = 2 * GR + 16;
-    if (gates) {
+    if constexpr (GATES) {
         const int cpr = GR / 8;  // 16-byte pieces a row
         for (int i = tid; i < 2 * W * cpr; i += NT) {
             const int r = i / cpr, c = i - r * cpr;
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(NT, (256 / NT) > 0 ? (256 / NT) : 1) step_kern
     const int Tb = a.accepted ? min(max(a.accepted[b], 0), a.T) : a.T;
     if (Tb > 0) load_token(0, cur);
     if (clustered) cluster_wait_acquire();  // every CTA's barriers and window reads
-    if (gates) {
+    if constexpr (GATES) {
         // The slab's 2W outputs: f of key channels slab W + o (o < W), which every slab
         // of the head needs for its decay, and z of its own value columns (o >= W); NT /
         // (2W) threads an output, 16-byte pieces of the rank taken round robin.
@@ -872,10 +874,12 @@ __global__ void __launch_bounds__(NW * 32) wstep_kernel(const StepArgs a)
 struct Variant {
     int D, W, NT;
     void (*fn)(StepArgs);
+    void (*fn_gates)(StepArgs);  // with the in-kernel low-rank gates
     const char *name;
 };
 
-#define GDN_VARIANT(D, W, NT) {D, W, NT, step_kernel<D, W, NT>, "step<" #D "," #W ">"}
+#define GDN_VARIANT(D, W, NT) \
+    {D, W, NT, step_kernel<D, W, NT, false>, step_kernel<D, W, NT, true>, "step<" #D "," #W ">"}
 const Variant kVariants[] = {
     GDN_VARIANT(128, 128, 256), GDN_VARIANT(128, 64, 256), GDN_VARIANT(128, 32, 128),
     GDN_VARIANT(128, 16, 64),   GDN_VARIANT(64, 64, 128),  GDN_VARIANT(64, 32, 64),
@@ -980,7 +984,7 @@ cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaS
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, v->fn, a);
+    return cudaLaunchKernelEx(&cfg, a.gate_lr ? v->fn_gates : v->fn, a);
 }
 
 namespace {
