@@ -4,12 +4,17 @@
 // recurrence) as about 90% of a KDA layer's decode time, all of it weight
 // streaming; "llama.cpp PR #84" runs f_a beside g_a (and beta) and f_b beside
 // g_b as single launches.  Here the q/k/v rows, f_a, g_a and beta share one
-// launch (one pass over x), and f_b and g_b another.
+// launch (one pass over x), and f_b and g_b another (or, on the column-slab step
+// kernel, the step itself: gdn_step.cu).
 //
 // y[b][n] = sum_k x[b][k] W[n][k]: W is bf16, row-major [N][K], streamed from
-// HBM once per 8 batch rows; x is fp32 or bf16 (a few rows, L2-resident); y is
-// fp32.  A launch serves up to four slots, each its own (W, x, y); the grid
-// covers all rows of all slots, a warp (or less) per row reading K in 16-byte pieces.
+// HBM once per pass over the batch rows; x is fp32 or bf16 (a few rows,
+// L2-resident); y is fp32.  A launch serves up to four slots, each its own
+// (W, x, y).  launch_proj picks one of four kernels by batch rows and K:
+//   * proj_tc_kernel (tcgen05, from 16 batch rows);
+//   * proj_mma_kernel (warp-level MMA, up to 8 bf16 / 4 fp32 rows shared by the slots);
+//   * proj_ring_kernel (CUDA cores, bulk-copy rings, rows of 1024 to 4096);
+//   * proj_kernel (CUDA cores, a warp or less per row, the rest).
 // Every launch uses programmatic dependent launch, so the next kernel's CTAs start
 // beside this one's and the weight stream can begin before the activations exist.
 #include <cuda_bf16.h>
