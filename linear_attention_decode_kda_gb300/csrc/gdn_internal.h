@@ -48,7 +48,9 @@ inline int slab_gate_smem(int D, int W, int R)
     (void)D;
     return 2 * W * (2 * R + 16) + 8 * R;
 }
-constexpr int kSlabGateSmemMax = 48 * 1024;
+// at most this much (the kernels' static shared memory is under 12 KB; the opt-in
+// limit is 227 KB): past it the gate pair runs as a launch of its own
+constexpr int kSlabGateSmemMax = 96 * 1024;
 
 // One launch configuration of the step kernels.
 struct StepPlan {

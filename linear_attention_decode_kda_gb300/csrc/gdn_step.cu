@@ -965,6 +965,19 @@ cudaError_t launch_slab(const StepPlan &plan, const StepArgs &a, bool pdl, cudaS
             !a.w_fb || !a.w_gb || (reinterpret_cast<uintptr_t>(a.w_fb) & 15u) ||
             (reinterpret_cast<uintptr_t>(a.w_gb) & 15u))
             return cudaErrorInvalidValue;
+        // static plus dynamic shared memory may pass the default 48 KB: opt in once per
+        // device and variant (benign race: every writer sets the same value)
+        static bool opted[64][sizeof(kVariants) / sizeof(kVariants[0])];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        const size_t vi = static_cast<size_t>(v - kVariants);
+        if (!opted[dev][vi]) {
+            e = cudaFuncSetAttribute(v->fn_gates, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlabGateSmemMax);
+            if (e != cudaSuccess) return e;
+            opted[dev][vi] = true;
+        }
         cfg.dynamicSmemBytes = static_cast<size_t>(gs);
     }
     cfg.stream = stream;

@@ -112,3 +112,14 @@ def test_layer_decode_repeat_is_bitwise():
     b = _run(shape, 1024, 64, seed=110)
     for u, v in zip(a, b):
         assert torch.equal(u, v)
+
+
+def test_layer_decode_in_step_gates_past_48kb():
+    """Eight value heads on one qk head: a whole head a CTA (step<128,128>), whose gate
+    rows at rank 128 take 70 KB of shared memory, past the default 48 KB."""
+    shape = synth.Shape(B=2, T=1, H_qk=1, H_v=8, d_k=128, d_v=128, kda=True)
+    s = dataclasses.replace(shape, bf16_in=False)
+    sh = gdn.make_shape(s.B, s.T, s.H_qk, s.H_v, s.d_k, s.d_v, kda=True, bf16_in=False,
+                        q_scale=s.q_scale)
+    assert gdn.gdn_kernel_variant(sh, gdn.OP_DECODE) == "step<128,128>"
+    _run(shape, 1024, 128, seed=120)
