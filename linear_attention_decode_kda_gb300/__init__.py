@@ -168,10 +168,13 @@ def gdn_layer_workspace_bytes(shape: GdnShape, weights: GdnLayerWeights) -> int:
 
 
 def layer_weights_from_torch(d_model: int, rank: int, **w) -> GdnLayerWeights:
-    """Weights as bf16 device tensors (keyword per field of GdnLayerWeights)."""
-    return GdnLayerWeights(d_model=d_model, rank=rank,
-                           **{k: _ptr(w[k]) for k in ("w_qkv", "w_fa", "w_fb", "w_ga", "w_gb",
-                                                      "w_beta", "w_o")})
+    """Weights as bf16 device tensors (keyword per field of GdnLayerWeights).  The
+    returned struct holds references to the tensors, so their memory outlives it."""
+    lw = GdnLayerWeights(d_model=d_model, rank=rank,
+                         **{k: _ptr(w[k]) for k in ("w_qkv", "w_fa", "w_fb", "w_ga", "w_gb",
+                                                    "w_beta", "w_o")})
+    lw._keep = dict(w)
+    return lw
 
 
 def gdn_prefill_workspace_bytes(shape: GdnShape) -> int:
@@ -216,7 +219,11 @@ def tensors_from_torch(*, qkv, f, beta, z, conv_w, A_log, dt_bias, norm_w, conv_
                     ("state_hist", state_hist), ("conv_hist", conv_hist)):
         if t is not None and hasattr(t, "is_contiguous") and not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    return GdnTensors(qkv=_ptr(qkv), f=_ptr(f), beta=_ptr(beta), z=_ptr(z), conv_w=_ptr(conv_w),
-                      A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), norm_w=_ptr(norm_w),
-                      conv_state=_ptr(conv_state), state=_ptr(state), out=_ptr(out),
-                      state_hist=_ptr(state_hist), conv_hist=_ptr(conv_hist))
+    t = GdnTensors(qkv=_ptr(qkv), f=_ptr(f), beta=_ptr(beta), z=_ptr(z), conv_w=_ptr(conv_w),
+                   A_log=_ptr(A_log), dt_bias=_ptr(dt_bias), norm_w=_ptr(norm_w),
+                   conv_state=_ptr(conv_state), state=_ptr(state), out=_ptr(out),
+                   state_hist=_ptr(state_hist), conv_hist=_ptr(conv_hist))
+    # the struct keeps its tensors alive (it holds only their addresses)
+    t._keep = (qkv, f, beta, z, conv_w, A_log, dt_bias, norm_w, conv_state, state, out,
+               state_hist, conv_hist)
+    return t

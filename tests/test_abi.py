@@ -286,3 +286,34 @@ def test_layer_decode_argument_checks(lib):
     assert call(s, weights(), ws_bytes=100) == gdn.GDN_ERR_WORKSPACE
     assert call(s, weights(), x=0x170008) == gdn.GDN_ERR_ALIGN
     assert call(s, weights(w_o=0x160004)) == gdn.GDN_ERR_ALIGN
+
+
+def test_abi_structs_keep_their_tensors_alive():
+    """The ABI structs hold raw addresses; the structs built from tensors keep those
+    tensors referenced, so a temporary passed in is not freed under a queued kernel."""
+    import gc
+    import weakref
+
+    import torch
+
+    w = {k: torch.zeros(64, dtype=torch.bfloat16) for k in
+         ("w_qkv", "w_fa", "w_fb", "w_ga", "w_gb", "w_beta", "w_o")}
+    refs = [weakref.ref(v) for v in w.values()]
+    lw = gdn.layer_weights_from_torch(8, 8, **w)
+    del w
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    assert lw.w_o == refs[-1]().data_ptr()
+
+    names = ("qkv", "f", "beta", "z", "conv_w", "A_log", "dt_bias", "norm_w", "conv_state",
+             "state", "out")
+    ts = {n: torch.zeros(16) for n in names}
+    trefs = [weakref.ref(v) for v in ts.values()]
+    tt = gdn.tensors_from_torch(**ts)
+    del ts
+    gc.collect()
+    assert all(r() is not None for r in trefs)
+    assert tt.state == trefs[names.index("state")]().data_ptr()
+    del lw, tt
+    gc.collect()
+    assert all(r() is None for r in refs + trefs)
